@@ -1,0 +1,423 @@
+"""Benchmark of the batched verify-and-accept step (one JSON line on rank 0).
+
+A step is one spec_verify call -- the streaming statistics pass plus the
+accept/sample pass -- over one batch of the B=64, K=4, V=128256 bf16
+workload (Zipf-like logits, T = 1), inputs resident in HBM.  Three copies of
+the inputs rotate (each 147.75 MB of logits, more than the 129 MB L2).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank verifies its own batch (its own seed) with no
+collective on the data path: weak scaling, value = all ranks' positions / the
+slowest rank's time.  ``--impl reference`` times the float64 CPU oracle on
+the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "spec_verify verified positions/s and HBM GB/s (% of roofline), B=64 K=4 V=128256"
+WORKLOAD = "llama3_stochastic"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--copies", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(w, accepted):
+    """Bytes the path must move for one batch: every target row, the draft rows
+    of rows with T > 0, and the re-read of the sampled position's rows
+    (2 rows on a rejection, 1 for a bonus; none for greedy rows)."""
+    elt = w.elt
+    V, K = w.V, w.K
+    stoch = w.temperature != 0
+    pass1 = w.B * (K + 1) * V * elt + int(stoch.sum()) * K * V * elt
+    rej = int(((accepted < K) & (accepted >= 0) & stoch).sum())
+    bonus = int(((accepted == K) & stoch).sum())
+    pass2 = (2 * rej + bonus) * V * elt
+    return pass1, pass2
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the GPU runs steps."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(os.path.join("/tmp", f"sv_clocks_{os.getpid()}.csv"), "w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.seek(0)
+        rows = [l.strip().split(", ") for l in self.out if l.strip()]
+        self.out.close()
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+_ORACLE_ROWS = None
+
+
+def _oracle_init(rows):
+    global _ORACLE_ROWS
+    _ORACLE_ROWS = rows
+
+
+def _oracle_job(idx):
+    from oracle import oracle
+    target, draft, tokens, unif, temp, dtype = _ORACLE_ROWS
+    r = [idx % len(temp)]
+    return oracle.spec_verify(target[r], draft[r], tokens[r], unif[r], temp[r],
+                              dtype=dtype).accepted_len
+
+
+def cpu_baseline(w, budget_s=12.0, sample_rows=4):
+    """The float64 oracle, as it stands, on the host cores over a bounded
+    sample: the first ``sample_rows`` rows of the batch, verified over and
+    over by a spawn pool (one worker per core) for about ``budget_s``."""
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    rows = (w.target[:sample_rows], w.draft[:sample_rows], w.draft_tokens[:sample_rows],
+            w.uniforms[:sample_rows], w.temperature[:sample_rows], w.dtype)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores, initializer=_oracle_init, initargs=(rows,)) as pool:
+        pool.map(_oracle_job, range(cores))   # warm the workers (imports)
+        t0 = time.perf_counter()
+        done = 0
+        for _ in pool.imap_unordered(_oracle_job, range(int(budget_s * cores * 100)), chunksize=1):
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        dt = time.perf_counter() - t0
+        pool.terminate()
+    return {"value": done * (w.K + 1) / dt, "unit": "positions/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{done} row verifications cycling over rows 0..{sample_rows - 1} of the "
+                      f"{w.name} batch (K={w.K}, V={w.V}), float64 numpy, {cores} spawn "
+                      f"workers, {dt:.1f} s wall"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from speculative_decoding_verification_25_gb300 import synth
+    from oracle import oracle
+    w = synth.make(args.workload, seed=args.seed, rows=range(8))
+    rows_per_step = 2
+
+    def step(i):
+        r = [(2 * i + k) % w.B for k in range(rows_per_step)]
+        oracle.spec_verify(w.target[r], w.draft[r], w.draft_tokens[r], w.uniforms[r],
+                           w.temperature[r], dtype=w.dtype)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    val = args.steps * rows_per_step * (w.K + 1) / dt
+    cfg = synth.WORKLOADS[args.workload]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "positions/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload} B={cfg['B']} K={cfg['K']} V={cfg['V']} "
+                               f"{cfg['dtype']}", "B": cfg["B"], "K": cfg["K"], "V": cfg["V"],
+                   "logits": cfg["dtype"], "step_sample_rows": rows_per_step},
+        "cpu_baseline": {"value": val, "unit": "positions/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows_per_step} rows of the batch per step, one process"},
+        "e2e": {"value": val, "unit": "positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_verification_25_gb300 import _native as N
+    from speculative_decoding_verification_25_gb300 import api, synth
+    from speculative_decoding_verification_25_gb300 import build as b
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("gloo")
+    b.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synth.make(args.workload, seed=args.seed + rank, workers=synth.default_workers())
+    dt_torch = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dtype_code = N.SV_BF16 if w.dtype == "bf16" else N.SV_F32
+    B, K, V = w.B, w.K, w.V
+
+    def host_logits(a):
+        t = torch.from_numpy(a.view(np.int16) if w.dtype == "bf16" else a)
+        return t.view(dt_torch) if w.dtype == "bf16" else t
+
+    host = dict(target=host_logits(w.target).pin_memory(), draft=host_logits(w.draft).pin_memory(),
+                draft_tokens=torch.from_numpy(w.draft_tokens).pin_memory(),
+                uniforms=torch.from_numpy(w.uniforms).pin_memory(),
+                temperature=torch.from_numpy(w.temperature).pin_memory())
+    copies = [{k: v.to(dev) for k, v in host.items()} for _ in range(args.copies)]
+    ws_bytes = N.spec_verify_workspace_bytes(B, K, V, dtype_code)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    outt = torch.empty(B, K + 1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def call(c):
+        st = N.spec_verify_raw(c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
+                               c["draft_tokens"].data_ptr(), c["uniforms"].data_ptr(),
+                               c["temperature"].data_ptr(), B, K, V, acc.data_ptr(),
+                               outt.data_ptr(), None, None, ws.data_ptr(), ws_bytes, sh)
+        if st != N.SV_OK:
+            raise N.SpecVerifyError(st)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- warm-up, then the timed region (device events on the launching stream)
+    for i in range(args.warmup):
+        call(copies[i % len(copies)])
+    sampler = ClockSampler(local)
+    sampler.start()
+    clock_t0 = time.perf_counter()
+    barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        call(copies[i % len(copies)])
+    ev1.record(stream)
+    barrier()
+    t_ms = max_over_ranks(ev0.elapsed_time(ev1))
+    gpu_launches = 2 * args.steps
+    accepted = acc.cpu().numpy()
+
+    # keep the GPU on the same steps for >= 1.5 s so the clock samples see load
+    i = 0
+    while time.perf_counter() - clock_t0 < 1.5:
+        call(copies[i % len(copies)])
+        i += 1
+        if i % 200 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+
+    # ---- per-kernel durations: the two stages with an event between them
+    n_split = max(args.steps, 50)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(n_split)]
+    barrier()
+    for i in range(n_split):
+        c = copies[i % len(copies)]
+        evs[i][0].record(stream)
+        st = N.spec_verify_row_stats_raw(c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
+                                         c["temperature"].data_ptr(), B, K, V, ws.data_ptr(),
+                                         ws_bytes, sh)
+        evs[i][1].record(stream)
+        st |= N.spec_verify_accept_sample_raw(
+            c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code, c["draft_tokens"].data_ptr(),
+            c["uniforms"].data_ptr(), c["temperature"].data_ptr(), B, K, V, acc.data_ptr(),
+            outt.data_ptr(), None, None, ws.data_ptr(), ws_bytes, sh)
+        evs[i][2].record(stream)
+        if st:
+            raise RuntimeError("stage call failed")
+    barrier()
+    k1 = [a.elapsed_time(m) for a, m, _ in evs]
+    k2 = [m.elapsed_time(e) for _, m, e in evs]
+    k1_ms = statistics.mean(k1)
+    k2_ms = statistics.mean(k2)
+
+    # ---- end to end through the public call with host buffers
+    d2h_acc = torch.empty(B, dtype=torch.int32).pin_memory()
+    d2h_tok = torch.empty(B, K + 1, dtype=torch.int32).pin_memory()
+    dst = copies[0]
+    e2e_steps = max(10, min(args.steps, 100))
+
+    def e2e_step():
+        for k in host:
+            dst[k].copy_(host[k], non_blocking=True)
+        r = api.spec_verify(dst["target"], dst["draft"], dst["draft_tokens"], dst["uniforms"],
+                            dst["temperature"], workspace=ws)
+        d2h_acc.copy_(r.accepted_len, non_blocking=True)
+        d2h_tok.copy_(r.out_tokens, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = d2h_acc.numel() * 4 + d2h_tok.numel() * 4
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    ms_per_step = t_ms / args.steps
+    positions = B * (K + 1) * world
+    value = positions / (ms_per_step * 1e-3)
+    p1_bytes, p2_bytes = algorithmic_bytes(w, accepted)
+    hbm, peak_src = peaks()
+    k1_gbs = p1_bytes / (k1_ms * 1e-3) / 1e9
+    step_gbs = (p1_bytes + p2_bytes) / (ms_per_step * 1e-3) / 1e9
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "row_stats_traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            with open(tr_path) as f:
+                tr = json.load(f)
+            if tr.get("workload") == args.workload and tr.get("kernel_rev") == kernel_rev():
+                traffic = tr.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+    cfg = synth.WORKLOADS[args.workload]
+    line = {
+        "metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload} B={B} K={K} V={V} {w.dtype} logits",
+                   "B": B, "K": K, "V": V, "logits": w.dtype, "T": "1.0 all rows",
+                   "l2": f"{len(copies)} rotating input copies of {w.logit_bytes() / 1e6:.2f} MB "
+                         f"(each larger than the 129 MB L2)",
+                   "parallelism": f"{world} independent replicas, own batch per GPU"},
+        "roofline": {"bound": "hbm", "achieved": k1_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": k1_gbs / hbm, "traffic": traffic,
+                     "kernel": "sv_row_stats_kernel", "peak_source": peak_src,
+                     "bytes_per_launch": p1_bytes, "ms_per_launch": k1_ms},
+        "step_roofline": {"achieved": step_gbs, "frac": step_gbs / hbm, "unit": "GB/s",
+                          "bytes_per_step": p1_bytes + p2_bytes,
+                          "accept_sample_ms_per_launch": k2_ms, "accept_sample_bytes": p2_bytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": positions / (e2e_ms * 1e-3), "unit": "positions/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+        "extra": {"rows_per_s": B * world / (ms_per_step * 1e-3),
+                  "emitted_tokens_per_step": int((accepted + 1).sum()),
+                  "mean_accepted_len": float(accepted.mean()),
+                  "peak_nominal_gbs": 8000.0, "frac_of_nominal": step_gbs / 8000.0},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def kernel_rev():
+    """Hash of the kernel sources: a stored ncu traffic figure is used only
+    while the kernels it was taken on are unchanged."""
+    import hashlib
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_25_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".inc")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

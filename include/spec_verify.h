@@ -1,0 +1,158 @@
+/*
+ * spec_verify -- batched verify-and-accept step of speculative decoding on
+ * one GB300 GPU (sm_103a).
+ *
+ * The operation is the exact rejection rule of speculative decoding as the
+ * lesson "Decodificação Especulativa e EAGLE" (ai-engineering.academy,
+ * phase 10 lesson 25) states it in its sections "A Regra de Exatidão"
+ * (the rule), "Caso ganancioso" (temperature 0) and "O Conceito / A
+ * Configuração com Dois Modelos" (steps 1-4: K drafted tokens, one target
+ * pass over K+1 positions, left-to-right acceptance, replacement or bonus
+ * token).  For every row b of the batch, with T = temperature[b]:
+ *
+ *   p_t = softmax(target_logits[b, t, :] / T)   t = 0..K
+ *   q_t = softmax(draft_logits[b, t, :] / T)    t = 0..K-1
+ *   x_t = draft_tokens[b, t],  r_t = uniforms[b, t],  u = uniforms[b, K]
+ *
+ *   for t = 0..K-1: accept x_t iff r_t * q_t(x_t) < p_t(x_t); at the first
+ *   rejection emit the smallest index i with C_i > u * W, C being the prefix
+ *   sum of the residual w = max(p_t - q_t, 0) and W its total, and stop.
+ *   If all K are accepted, emit the bonus token chosen the same way from p_K.
+ *   T == 0 (greedy): accept iff argmax(target_logits[b, t, :]) == x_t
+ *   (lowest index on ties); a rejection or the bonus emits that argmax.
+ *
+ * If the residual is zero everywhere (p == q to rounding) the replacement is
+ * drawn from p_t with u.  Logits may be -inf; NaN and +inf are outside the
+ * contract (no fault, unspecified tokens).
+ *
+ * Conventions for every entry point:
+ *   - all array pointers are DEVICE pointers unless stated otherwise; arrays
+ *     are dense, row-major, C-contiguous, owned by the caller;
+ *   - the library allocates no memory and keeps no state beyond a per-device
+ *     cache of the SM count and kernel attributes;
+ *   - work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and runs asynchronously: spec_verify never synchronises the
+ *     host; inputs must stay unchanged until the stream has run the call;
+ *   - host-detectable errors return a status before anything is launched;
+ *     row-level problems found on the device never fault or trap: the row is
+ *     written as an error row (accepted_len = -1, all out_tokens -1) and a
+ *     flag is OR-ed into the workspace (see spec_verify_device_errors).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* storage type of the logits */
+#define SV_F32 0   /* IEEE float32 */
+#define SV_BF16 1  /* bfloat16 (upper half of a float32) */
+
+/* status codes returned by the host entry points */
+#define SV_OK 0
+#define SV_ERR_NULL 1       /* a required pointer is NULL */
+#define SV_ERR_SHAPE 2      /* B < 0, K outside [1, SV_MAX_K], V outside [1, spec_verify_max_vocab(dtype)] */
+#define SV_ERR_DTYPE 3      /* dtype is neither SV_F32 nor SV_BF16 */
+#define SV_ERR_ALIGN 4      /* a pointer is not aligned to its element (workspace: 16 bytes) */
+#define SV_ERR_WORKSPACE 5  /* workspace_bytes < spec_verify_workspace_bytes(B, K, V, dtype) */
+#define SV_ERR_CUDA 6       /* a CUDA runtime call failed (launch, attribute, copy) */
+
+/* device-side row flags, OR-ed into the workspace error word */
+#define SV_DEV_BAD_TEMPERATURE 1u  /* T negative, NaN, infinite, or in (0, FLT_MIN) */
+#define SV_DEV_BAD_TOKEN 2u        /* a drafted token outside [0, V) */
+#define SV_DEV_NONFINITE 4u        /* a logit row without a finite maximum or sum */
+
+#define SV_MAX_K 16
+
+/*
+ * Bytes of scratch the caller must pass to spec_verify for this shape.
+ * Pure host arithmetic; returns 0 for invalid arguments.
+ */
+size_t spec_verify_workspace_bytes(int B, int K, int V, int dtype);
+
+/* Largest vocabulary accepted for `dtype` (0 for an unknown dtype). */
+int spec_verify_max_vocab(int dtype);
+
+/*
+ * The verify-and-accept step for a batch of B rows.
+ *
+ *   target_logits  [B, K+1, V] of `dtype`; element-aligned.  Rows whose base
+ *                  address and pitch (V * element size) are multiples of 16
+ *                  bytes take the vectorised path, others a scalar path.
+ *   draft_logits   [B, K, V] of `dtype` (not read for rows with T == 0).
+ *   draft_tokens   [B, K] int32, the drafted ids x_0..x_{K-1}.
+ *   uniforms       [B, K+1] float32 in [0, 1): r_0..r_{K-1}, then u.
+ *                  Not read for rows with T == 0.
+ *   temperature    [B] float32; 0 selects the greedy rule.
+ *   accepted_len   [B] int32 out: accepted drafted tokens, 0..K (-1 = error row).
+ *   out_tokens     [B, K+1] int32 out: x_0..x_{n-1}, then the replacement
+ *                  or bonus token at slot n = accepted_len; later slots -1.
+ *   logp_out       optional [B, K] float32 out (NULL to skip): log p_t(x_t)
+ *                  for every drafted position of rows with T > 0; NaN on
+ *                  greedy and error rows.
+ *   logq_out       optional [B, K] float32 out: log q_t(x_t), same layout.
+ *   workspace      device scratch, 16-byte aligned, at least
+ *                  spec_verify_workspace_bytes(B, K, V, dtype) bytes; its
+ *                  contents need no initialisation and are overwritten.
+ *   stream         cudaStream_t to enqueue on.
+ *
+ * B == 0 is a no-op (pointers may then be NULL).  Returns SV_OK or an
+ * SV_ERR_* code; on an error code nothing has been launched.  Two calls
+ * that share a workspace must be ordered on the device (same stream).
+ */
+int spec_verify(const void* target_logits, const void* draft_logits, int dtype,
+                const int32_t* draft_tokens, const float* uniforms,
+                const float* temperature, int B, int K, int V,
+                int32_t* accepted_len, int32_t* out_tokens,
+                float* logp_out, float* logq_out,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The two stages spec_verify runs, for callers that schedule them apart
+ * (or time them).  spec_verify_row_stats + spec_verify_accept_sample on the
+ * same stream, inputs and workspace give exactly spec_verify's result.
+ *
+ * spec_verify_row_stats streams every target row and the draft rows of
+ * rows with T > 0 once and leaves one partial per 4 KB tile in the
+ * workspace: (tile max m, sum of e^((x - m)/T)) for the softmax
+ * normaliser, or (max logit, its lowest index) for T == 0 rows.  It also
+ * clears the device flag word.
+ *
+ * spec_verify_accept_sample folds those partials into per-position
+ * statistics, runs the acceptance test and draws the replacement or bonus
+ * token (re-reading only the logit rows of the one position that needs a
+ * draw).  It is launched so that it may start while the previous kernel on
+ * the stream drains; it must follow spec_verify_row_stats on that stream.
+ * Arguments and return codes are those of spec_verify.
+ */
+int spec_verify_row_stats(const void* target_logits, const void* draft_logits, int dtype,
+                          const float* temperature, int B, int K, int V,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+int spec_verify_accept_sample(const void* target_logits, const void* draft_logits, int dtype,
+                              const int32_t* draft_tokens, const float* uniforms,
+                              const float* temperature, int B, int K, int V,
+                              int32_t* accepted_len, int32_t* out_tokens,
+                              float* logp_out, float* logq_out,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Reads the device-side row flags (SV_DEV_*) that the last spec_verify call
+ * on this workspace OR-ed in.  Enqueues a 4-byte copy on `stream` and
+ * SYNCHRONISES that stream; `flags` is a HOST pointer.  Returns SV_OK,
+ * SV_ERR_NULL or SV_ERR_CUDA.
+ */
+int spec_verify_device_errors(const void* workspace, void* stream, uint32_t* flags);
+
+/* Static, NUL-terminated description of a status code. */
+const char* spec_verify_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

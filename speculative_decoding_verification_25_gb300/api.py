@@ -1,0 +1,100 @@
+"""Torch-facing wrapper of the C ABI.  PyTorch supplies device memory and
+streams; the verify step itself runs in the library's kernels.
+
+    accepted_len, out_tokens = spec_verify(target, draft, draft_tokens,
+                                           uniforms, temperature)
+
+``target`` [B, K+1, V] and ``draft`` [B, K, V] are CUDA tensors of
+torch.bfloat16 or torch.float32; ``draft_tokens`` [B, K] int32;
+``uniforms`` [B, K+1] float32; ``temperature`` [B] float32 (0 = greedy).
+"""
+from __future__ import annotations
+
+from typing import NamedTuple, Optional
+
+import torch
+
+from . import _native as N
+
+_DTYPES = {torch.bfloat16: N.SV_BF16, torch.float32: N.SV_F32}
+_workspaces: dict = {}
+
+
+class VerifyResult(NamedTuple):
+    accepted_len: torch.Tensor           # [B] int32, -1 = error row
+    out_tokens: torch.Tensor             # [B, K+1] int32, -1 padded
+    logp: Optional[torch.Tensor] = None  # [B, K] float32 log p_t(x_t)
+    logq: Optional[torch.Tensor] = None  # [B, K] float32 log q_t(x_t)
+
+
+def _check(t: torch.Tensor, name: str, dtype=None, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace_for(B: int, K: int, V: int, dtype: int, device: torch.device) -> torch.Tensor:
+    """A cached device workspace large enough for this shape."""
+    need = N.spec_verify_workspace_bytes(B, K, V, dtype)
+    if need == 0:
+        raise ValueError(f"invalid shape B={B} K={K} V={V}")
+    key = (device.index if device.index is not None else torch.cuda.current_device())
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(max(need, 1 << 20), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def spec_verify(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor,
+                uniforms: torch.Tensor, temperature: torch.Tensor, *,
+                want_logprobs: bool = False, out: Optional[VerifyResult] = None,
+                workspace: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> VerifyResult:
+    """Verify a batch on the current (or given) CUDA stream; no host sync."""
+    if target.dim() != 3:
+        raise ValueError("target must be [B, K+1, V]")
+    B, K1, V = target.shape
+    K = K1 - 1
+    dev = target.device
+    if target.dtype not in _DTYPES:
+        raise TypeError(f"target dtype {target.dtype} is not bfloat16 or float32")
+    dt = _DTYPES[target.dtype]
+    _check(target, "target", device=dev)
+    _check(draft, "draft", dtype=target.dtype, shape=(B, K, V), device=dev)
+    _check(draft_tokens, "draft_tokens", dtype=torch.int32, shape=(B, K), device=dev)
+    _check(uniforms, "uniforms", dtype=torch.float32, shape=(B, K + 1), device=dev)
+    _check(temperature, "temperature", dtype=torch.float32, shape=(B,), device=dev)
+    if out is None:
+        out = VerifyResult(
+            torch.empty(B, dtype=torch.int32, device=dev),
+            torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+            torch.empty(B, K, dtype=torch.float32, device=dev) if want_logprobs else None,
+            torch.empty(B, K, dtype=torch.float32, device=dev) if want_logprobs else None)
+    if workspace is None:
+        workspace = workspace_for(B, K, V, dt, dev)
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    status = N.spec_verify_raw(
+        target.data_ptr(), draft.data_ptr(), dt, draft_tokens.data_ptr(), uniforms.data_ptr(),
+        temperature.data_ptr(), B, K, V, out.accepted_len.data_ptr(), out.out_tokens.data_ptr(),
+        out.logp.data_ptr() if out.logp is not None else None,
+        out.logq.data_ptr() if out.logq is not None else None,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), st.cuda_stream)
+    if status != N.SV_OK:
+        raise N.SpecVerifyError(status)
+    return out
+
+
+def device_errors(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
+    """SV_DEV_* flags of the last call on ``workspace`` (synchronises the stream)."""
+    st = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+    return N.spec_verify_device_errors(workspace.data_ptr(), st.cuda_stream)

@@ -1,0 +1,318 @@
+// Host side of spec_verify: argument checks, launch geometry and the C ABI
+// declared in include/spec_verify.h.
+//
+// One call = two launches on the caller's stream:
+//   1. sv_row_stats_kernel, a persistent grid (SM count x resident CTAs)
+//      whose warps stream contiguous ranges of 4 KB row tiles;
+//   2. sv_accept_sample_kernel, one thread-block cluster per batch row,
+//      launched with programmatic dependent launch so its CTAs are resident
+//      and waiting when the streaming pass retires.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "spec_verify.h"
+#include "sv_kernels.cuh"
+
+namespace {
+
+constexpr size_t kHeaderBytes = 256;   // device error word lives at offset 0
+constexpr int kMaxDevices = 64;
+
+struct DeviceCache {
+  std::once_flag once;
+  int sm_count = 0;
+  int row_stats_blocks_per_sm[2][2] = {{0, 0}, {0, 0}};  // [dtype][aligned]
+  cudaError_t init_error = cudaSuccess;
+};
+
+DeviceCache g_devices[kMaxDevices];
+
+int vec_of(int dtype) { return dtype == SV_BF16 ? 8 : 4; }
+int elt_of(int dtype) { return dtype == SV_BF16 ? 2 : 4; }
+
+bool shape_ok(int B, int K, int V, int dtype) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return false;
+  if (B < 0 || K < 1 || K > SV_MAX_K || V < 1) return false;
+  return V <= spec_verify_max_vocab(dtype);
+}
+
+long long tiles_per_row(int V, int dtype) {
+  const long long tile_elems = (long long)sv::kTileVecs * vec_of(dtype);
+  return (V + tile_elems - 1) / tile_elems;
+}
+
+template <typename E, bool kAligned>
+void* row_stats_fn() {
+  return (void*)sv::sv_row_stats_kernel<E, kAligned>;
+}
+template <typename E, bool kAligned>
+void* accept_fn() {
+  return (void*)sv::sv_accept_sample_kernel<E, kAligned>;
+}
+
+void* pick_row_stats(int dtype, bool aligned) {
+  if (dtype == SV_BF16) return aligned ? row_stats_fn<sv::Bf16, true>() : row_stats_fn<sv::Bf16, false>();
+  return aligned ? row_stats_fn<sv::F32, true>() : row_stats_fn<sv::F32, false>();
+}
+void* pick_accept(int dtype, bool aligned) {
+  if (dtype == SV_BF16) return aligned ? accept_fn<sv::Bf16, true>() : accept_fn<sv::Bf16, false>();
+  return aligned ? accept_fn<sv::F32, true>() : accept_fn<sv::F32, false>();
+}
+
+// SM count, occupancy of the streaming kernel, and the shared-memory limit
+// of the sampling kernel; once per device.
+DeviceCache* device_cache(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceCache& dc = g_devices[dev];
+  std::call_once(dc.once, [&dc, dev]() {
+    cudaError_t e = cudaDeviceGetAttribute(&dc.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    for (int dt = 0; dt < 2 && e == cudaSuccess; ++dt) {
+      for (int al = 0; al < 2 && e == cudaSuccess; ++al) {
+        int nb = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, pick_row_stats(dt, al != 0),
+                                                          sv::kP1Threads, 0);
+        dc.row_stats_blocks_per_sm[dt][al] = nb > 0 ? nb : 1;
+        if (e == cudaSuccess) {
+          e = cudaFuncSetAttribute(pick_accept(dt, al != 0),
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   sv::kMaxVecsPerCta * (int)sizeof(float4));
+        }
+      }
+    }
+    dc.init_error = e;
+  });
+  return &dc;
+}
+
+// Cluster size for the sampling step: enough CTAs that each owns at most
+// 2048 vectors of the sampled row, at most 8.
+void cluster_geometry(int V, int dtype, int* cs, int* nvec, int* vpc) {
+  const int vec = vec_of(dtype);
+  *nvec = (V + vec - 1) / vec;
+  int c = 1;
+  while (c < sv::kMaxClusterSize && (*nvec + c - 1) / c > 2048) c *= 2;
+  *cs = c;
+  *vpc = (*nvec + c - 1) / c;
+}
+
+bool aligned_to(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+}  // namespace
+
+namespace {
+
+// Checks shared by every launching entry point; SV_OK means the arguments
+// are usable (B may be 0).
+int validate(const void* target_logits, const void* draft_logits, int dtype,
+             const int32_t* draft_tokens, const float* uniforms, const float* temperature,
+             int B, int K, int V, const int32_t* accepted_len, const int32_t* out_tokens,
+             const float* logp_out, const float* logq_out, const void* workspace,
+             size_t workspace_bytes, bool need_outputs) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (!shape_ok(B, K, V, dtype)) return SV_ERR_SHAPE;
+  if (B == 0) return SV_OK;
+  if (!target_logits || !draft_logits || !temperature || !workspace) return SV_ERR_NULL;
+  if (need_outputs && (!draft_tokens || !uniforms || !accepted_len || !out_tokens))
+    return SV_ERR_NULL;
+  const size_t elt = (size_t)elt_of(dtype);
+  if (!aligned_to(target_logits, elt) || !aligned_to(draft_logits, elt) ||
+      !aligned_to(temperature, 4) || !aligned_to(workspace, 16))
+    return SV_ERR_ALIGN;
+  if (need_outputs &&
+      (!aligned_to(draft_tokens, 4) || !aligned_to(uniforms, 4) || !aligned_to(accepted_len, 4) ||
+       !aligned_to(out_tokens, 4) || (logp_out && !aligned_to(logp_out, 4)) ||
+       (logq_out && !aligned_to(logq_out, 4))))
+    return SV_ERR_ALIGN;
+  if (workspace_bytes < spec_verify_workspace_bytes(B, K, V, dtype)) return SV_ERR_WORKSPACE;
+  return SV_OK;
+}
+
+bool vector_path(const void* target_logits, const void* draft_logits, int V, int dtype) {
+  return aligned_to(target_logits, 16) && aligned_to(draft_logits, 16) &&
+         ((size_t)V * (size_t)elt_of(dtype)) % 16 == 0;
+}
+
+int launch_row_stats(const void* target_logits, const void* draft_logits, int dtype,
+                     const float* temperature, int B, int K, int V, void* workspace,
+                     DeviceCache* dc, cudaStream_t st) {
+  const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
+  const long long tpr = tiles_per_row(V, dtype);
+  const long long n_target_rows = (long long)B * (K + 1);
+  sv::RowStatsArgs ra;
+  ra.target = target_logits;
+  ra.draft = draft_logits;
+  ra.temperature = temperature;
+  ra.B = B;
+  ra.K = K;
+  ra.V = V;
+  ra.tiles_per_row = (int)tpr;
+  ra.n_tiles = (n_target_rows + (long long)B * K) * tpr;
+  ra.n_target_rows = n_target_rows;
+  ra.partials = (float2*)((char*)workspace + kHeaderBytes);
+  ra.err = (unsigned*)workspace;
+  // persistent grid: every SM filled once; every warp a contiguous tile range
+  const int warps_per_block = sv::kP1Threads / 32;
+  long long blocks = (long long)dc->sm_count * dc->row_stats_blocks_per_sm[dtype][aligned ? 1 : 0];
+  const long long need = (ra.n_tiles + warps_per_block - 1) / warps_per_block;
+  if (blocks > need) blocks = need;
+  if (blocks < 1) blocks = 1;
+  void* args[] = {&ra};
+  return cudaLaunchKernel(pick_row_stats(dtype, aligned), dim3((unsigned)blocks),
+                          dim3(sv::kP1Threads), args, 0, st) == cudaSuccess
+             ? SV_OK
+             : SV_ERR_CUDA;
+}
+
+int launch_accept_sample(const void* target_logits, const void* draft_logits, int dtype,
+                         const int32_t* draft_tokens, const float* uniforms,
+                         const float* temperature, int B, int K, int V, int32_t* accepted_len,
+                         int32_t* out_tokens, float* logp_out, float* logq_out, void* workspace,
+                         cudaStream_t st) {
+  const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
+  int cs, nvec, vpc;
+  cluster_geometry(V, dtype, &cs, &nvec, &vpc);
+  sv::AcceptArgs aa;
+  aa.target = target_logits;
+  aa.draft = draft_logits;
+  aa.tokens = draft_tokens;
+  aa.uniforms = uniforms;
+  aa.temperature = temperature;
+  aa.B = B;
+  aa.K = K;
+  aa.V = V;
+  aa.tiles_per_row = (int)tiles_per_row(V, dtype);
+  aa.n_target_rows = (long long)B * (K + 1);
+  aa.nvec = nvec;
+  aa.vecs_per_cta = vpc;
+  aa.partials = (const float2*)((const char*)workspace + kHeaderBytes);
+  aa.err = (unsigned*)workspace;
+  aa.accepted_len = accepted_len;
+  aa.out_tokens = out_tokens;
+  aa.logp_out = logp_out;
+  aa.logq_out = logq_out;
+  void* args[] = {&aa};
+
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)B * (unsigned)cs);
+  cfg.blockDim = dim3(sv::kP2Threads);
+  cfg.dynamicSmemBytes = (size_t)vpc * sizeof(float4);
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = (unsigned)cs;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelExC(&cfg, pick_accept(dtype, aligned), args);
+  if (e != cudaSuccess) {
+    // without the early-launch overlap the dependency is plain stream order
+    (void)cudaGetLastError();
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, pick_accept(dtype, aligned), args);
+  }
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+DeviceCache* current_device_cache() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  DeviceCache* dc = device_cache(dev);
+  if (!dc || dc->init_error != cudaSuccess) return nullptr;
+  return dc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_max_vocab(int dtype) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return 0;
+  // every CTA of the cluster keeps 16 bytes of shared memory per vector it owns
+  return sv::kMaxClusterSize * sv::kMaxVecsPerCta * vec_of(dtype);
+}
+
+size_t spec_verify_workspace_bytes(int B, int K, int V, int dtype) {
+  if (!shape_ok(B, K, V, dtype)) return 0;
+  const long long rows = (long long)B * (K + 1) + (long long)B * K;
+  return kHeaderBytes + (size_t)(rows * tiles_per_row(V, dtype)) * sizeof(float2);
+}
+
+const char* spec_verify_status_string(int status) {
+  switch (status) {
+    case SV_OK: return "ok";
+    case SV_ERR_NULL: return "a required pointer is NULL";
+    case SV_ERR_SHAPE: return "B, K or V out of range";
+    case SV_ERR_DTYPE: return "unknown logit dtype";
+    case SV_ERR_ALIGN: return "a pointer is not aligned to its element size (workspace: 16 bytes)";
+    case SV_ERR_WORKSPACE: return "workspace smaller than spec_verify_workspace_bytes()";
+    case SV_ERR_CUDA: return "a CUDA runtime call failed";
+    default: return "unknown status";
+  }
+}
+
+int spec_verify_row_stats(const void* target_logits, const void* draft_logits, int dtype,
+                          const float* temperature, int B, int K, int V, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  const int st = validate(target_logits, draft_logits, dtype, nullptr, nullptr, temperature, B, K,
+                          V, nullptr, nullptr, nullptr, nullptr, workspace, workspace_bytes, false);
+  if (st != SV_OK || B == 0) return st;
+  DeviceCache* dc = current_device_cache();
+  if (!dc) return SV_ERR_CUDA;
+  return launch_row_stats(target_logits, draft_logits, dtype, temperature, B, K, V, workspace, dc,
+                          (cudaStream_t)stream);
+}
+
+int spec_verify_accept_sample(const void* target_logits, const void* draft_logits, int dtype,
+                              const int32_t* draft_tokens, const float* uniforms,
+                              const float* temperature, int B, int K, int V,
+                              int32_t* accepted_len, int32_t* out_tokens, float* logp_out,
+                              float* logq_out, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  const int st = validate(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                          B, K, V, accepted_len, out_tokens, logp_out, logq_out, workspace,
+                          workspace_bytes, true);
+  if (st != SV_OK || B == 0) return st;
+  if (!current_device_cache()) return SV_ERR_CUDA;
+  return launch_accept_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
+                              temperature, B, K, V, accepted_len, out_tokens, logp_out, logq_out,
+                              workspace, (cudaStream_t)stream);
+}
+
+int spec_verify(const void* target_logits, const void* draft_logits, int dtype,
+                const int32_t* draft_tokens, const float* uniforms, const float* temperature,
+                int B, int K, int V, int32_t* accepted_len, int32_t* out_tokens,
+                float* logp_out, float* logq_out, void* workspace, size_t workspace_bytes,
+                void* stream) {
+  const int st = validate(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                          B, K, V, accepted_len, out_tokens, logp_out, logq_out, workspace,
+                          workspace_bytes, true);
+  if (st != SV_OK || B == 0) return st;
+  DeviceCache* dc = current_device_cache();
+  if (!dc) return SV_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int r = launch_row_stats(target_logits, draft_logits, dtype, temperature, B, K, V,
+                                 workspace, dc, s);
+  if (r != SV_OK) return r;
+  return launch_accept_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
+                              temperature, B, K, V, accepted_len, out_tokens, logp_out, logq_out,
+                              workspace, s);
+}
+
+int spec_verify_device_errors(const void* workspace, void* stream, uint32_t* flags) {
+  if (!workspace || !flags) return SV_ERR_NULL;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_OK;
+}
+
+}  // extern "C"

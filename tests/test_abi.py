@@ -1,0 +1,120 @@
+"""The C ABI on the host: the library loads without a GPU, exports every
+function include/spec_verify.h declares, and rejects bad arguments with a
+status before anything is launched (no call here reaches the GPU)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def N():
+    from speculative_decoding_verification_25_gb300 import build as b
+    b.build()
+    from speculative_decoding_verification_25_gb300 import _native
+    _native.load()
+    return _native
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M):
+            if not m.group(0).lstrip().startswith(("#", "if", "return")):
+                names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for required in ("spec_verify", "spec_verify_workspace_bytes", "spec_verify_status_string",
+                     "spec_verify_device_errors", "spec_verify_max_vocab"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(N):
+    lib = ctypes.CDLL(N.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert set(_declared_functions()) <= set(N._SIG)
+
+
+def test_workspace_bytes_arithmetic(N):
+    # 256-byte header + 8 bytes per 4 KB tile of every target and draft row
+    B, K, V = 64, 4, 128256
+    tiles = -(-V // 2048)
+    assert N.spec_verify_workspace_bytes(B, K, V, N.SV_BF16) == 256 + (B * (K + 1) + B * K) * tiles * 8
+    tiles32 = -(-V // 1024)
+    assert N.spec_verify_workspace_bytes(B, K, V, N.SV_F32) == 256 + (B * (K + 1) + B * K) * tiles32 * 8
+    assert N.spec_verify_workspace_bytes(0, 4, 1000, N.SV_F32) == 256
+    for bad in ((-1, 4, 10, 0), (1, 0, 10, 0), (1, 17, 10, 0), (1, 4, 0, 0), (1, 4, 10, 2),
+                (1, 4, N.spec_verify_max_vocab(0) + 1, 0)):
+        assert N.spec_verify_workspace_bytes(*bad) == 0
+
+
+def test_max_vocab_covers_the_workloads(N):
+    assert N.spec_verify_max_vocab(N.SV_BF16) >= 262144
+    assert N.spec_verify_max_vocab(N.SV_F32) >= 262144
+    assert N.spec_verify_max_vocab(7) == 0
+
+
+def test_status_strings(N):
+    for s in range(7):
+        assert N.status_string(s)
+    assert N.status_string(99) == "unknown status"
+
+
+FAKE = 0x10000   # never dereferenced: every call below fails validation first
+
+
+def _call(N, **kw):
+    args = dict(target=FAKE, draft=FAKE, dtype=N.SV_BF16, tokens=FAKE, uniforms=FAKE,
+                temperature=FAKE, B=2, K=4, V=1024, accepted=FAKE, out=FAKE, logp=None,
+                logq=None, ws=FAKE, ws_bytes=1 << 30, stream=None)
+    args.update(kw)
+    return N.spec_verify_raw(args["target"], args["draft"], args["dtype"], args["tokens"],
+                             args["uniforms"], args["temperature"], args["B"], args["K"],
+                             args["V"], args["accepted"], args["out"], args["logp"],
+                             args["logq"], args["ws"], args["ws_bytes"], args["stream"])
+
+
+def test_validation_errors_launch_nothing(N):
+    assert _call(N, dtype=5) == N.SV_ERR_DTYPE
+    assert _call(N, B=-1) == N.SV_ERR_SHAPE
+    assert _call(N, K=0) == N.SV_ERR_SHAPE
+    assert _call(N, K=17) == N.SV_ERR_SHAPE
+    assert _call(N, V=0) == N.SV_ERR_SHAPE
+    assert _call(N, V=N.spec_verify_max_vocab(N.SV_BF16) + 1) == N.SV_ERR_SHAPE
+    for field in ("target", "draft", "tokens", "uniforms", "temperature", "accepted", "out", "ws"):
+        assert _call(N, **{field: None}) == N.SV_ERR_NULL, field
+    assert _call(N, target=FAKE + 1) == N.SV_ERR_ALIGN          # bf16 needs 2-byte alignment
+    assert _call(N, dtype=N.SV_F32, draft=FAKE + 2) == N.SV_ERR_ALIGN
+    assert _call(N, tokens=FAKE + 2) == N.SV_ERR_ALIGN
+    assert _call(N, logp=FAKE + 1) == N.SV_ERR_ALIGN
+    assert _call(N, ws=FAKE + 8) == N.SV_ERR_ALIGN
+    need = N.spec_verify_workspace_bytes(2, 4, 1024, N.SV_BF16)
+    assert _call(N, ws_bytes=need - 1) == N.SV_ERR_WORKSPACE
+
+
+def test_empty_batch_is_a_no_op(N):
+    assert _call(N, B=0, target=None, draft=None, tokens=None, uniforms=None, temperature=None,
+                 accepted=None, out=None, ws=None, ws_bytes=0) == N.SV_OK
+
+
+def test_device_errors_rejects_null(N):
+    flags = ctypes.c_uint32(0)
+    assert N.load().spec_verify_device_errors(None, None, ctypes.byref(flags)) == N.SV_ERR_NULL
+    assert N.load().spec_verify_device_errors(FAKE, None, None) == N.SV_ERR_NULL
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    from speculative_decoding_verification_25_gb300 import _native
+    monkeypatch.setattr(_native, "_lib", None)
+    monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(ImportError):
+        _native.load()
