@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--copies", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="warm-up and timed steps only (for ncu captures); prints ms/step")
     return ap.parse_args()
 
 
@@ -276,6 +278,13 @@ def run_ours(args):
     t_ms = max_over_ranks(ev0.elapsed_time(ev1))
     gpu_launches = 2 * args.steps
     accepted = acc.cpu().numpy()
+    if args.profile:
+        sampler.stop()
+        if rank == 0:
+            print(json.dumps({"profile": True, "ms_per_step": t_ms / args.steps}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     # keep the GPU on the same steps for >= 1.5 s so the clock samples see load
     i = 0

@@ -63,6 +63,12 @@ void* pick_accept(int dtype, bool aligned) {
   return aligned ? accept_fn<sv::F32, true>() : accept_fn<sv::F32, false>();
 }
 
+// dynamic shared memory of the accept/sample kernel: 16 B of per-group
+// weights for every group of the sampled row the CTA owns
+size_t accept_smem_bytes(int groups_per_cta) { return (size_t)groups_per_cta * 16; }
+
+constexpr int kMaxGroupsPerCta = sv::kMaxGroupsPerThread * sv::kP2Threads;
+
 // SM count, occupancy of the streaming kernel, and the shared-memory limit
 // of the sampling kernel; once per device.
 DeviceCache* device_cache(int dev) {
@@ -76,11 +82,12 @@ DeviceCache* device_cache(int dev) {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, pick_row_stats(dt, al != 0),
                                                           sv::kP1Threads, 0);
         dc.row_stats_blocks_per_sm[dt][al] = nb > 0 ? nb : 1;
-        if (e == cudaSuccess) {
-          e = cudaFuncSetAttribute(pick_accept(dt, al != 0),
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   sv::kMaxVecsPerCta * (int)sizeof(float4));
-        }
+        void* ac = pick_accept(dt, al != 0);
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(ac, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)accept_smem_bytes(kMaxGroupsPerCta));
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(ac, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       }
     }
     dc.init_error = e;
@@ -88,15 +95,16 @@ DeviceCache* device_cache(int dev) {
   return &dc;
 }
 
-// Cluster size for the sampling step: enough CTAs that each owns at most
-// 2048 vectors of the sampled row, at most 8.
-void cluster_geometry(int V, int dtype, int* cs, int* nvec, int* vpc) {
-  const int vec = vec_of(dtype);
-  *nvec = (V + vec - 1) / vec;
+// Cluster size for the sampling step: the smallest power of two for which
+// every CTA owns at most two groups per thread, at most 16 (16 needs the
+// non-portable cluster size, allowed at initialisation).
+void cluster_geometry(int V, int dtype, int* cs, int* ngroups, int* gpc) {
+  const int gelems = sv::kGroupVecs * vec_of(dtype);
+  *ngroups = (V + gelems - 1) / gelems;
   int c = 1;
-  while (c < sv::kMaxClusterSize && (*nvec + c - 1) / c > 2048) c *= 2;
+  while (c < sv::kMaxClusterSize && (*ngroups + c - 1) / c > 2 * sv::kP2Threads) c *= 2;
   *cs = c;
-  *vpc = (*nvec + c - 1) / c;
+  *gpc = (*ngroups + c - 1) / c;
 }
 
 bool aligned_to(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
@@ -151,18 +159,19 @@ int launch_row_stats(const void* target_logits, const void* draft_logits, int dt
   ra.V = V;
   ra.tiles_per_row = (int)tpr;
   ra.n_tiles = (n_target_rows + (long long)B * K) * tpr;
-  ra.n_target_rows = n_target_rows;
+  ra.n_target_rows = (int)n_target_rows;
   ra.partials = (float2*)((char*)workspace + kHeaderBytes);
   ra.err = (unsigned*)workspace;
   // persistent grid: every SM filled once; every warp a contiguous tile range
-  const int warps_per_block = sv::kP1Threads / 32;
+  const int threads = sv::kP1Threads;
+  const int warps_per_block = threads / 32;
   long long blocks = (long long)dc->sm_count * dc->row_stats_blocks_per_sm[dtype][aligned ? 1 : 0];
   const long long need = (ra.n_tiles + warps_per_block - 1) / warps_per_block;
   if (blocks > need) blocks = need;
   if (blocks < 1) blocks = 1;
   void* args[] = {&ra};
-  return cudaLaunchKernel(pick_row_stats(dtype, aligned), dim3((unsigned)blocks),
-                          dim3(sv::kP1Threads), args, 0, st) == cudaSuccess
+  return cudaLaunchKernel(pick_row_stats(dtype, aligned), dim3((unsigned)blocks), dim3(threads),
+                          args, 0, st) == cudaSuccess
              ? SV_OK
              : SV_ERR_CUDA;
 }
@@ -173,8 +182,8 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
                          int32_t* out_tokens, float* logp_out, float* logq_out, void* workspace,
                          cudaStream_t st) {
   const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
-  int cs, nvec, vpc;
-  cluster_geometry(V, dtype, &cs, &nvec, &vpc);
+  int cs, ngroups, gpc;
+  cluster_geometry(V, dtype, &cs, &ngroups, &gpc);
   sv::AcceptArgs aa;
   aa.target = target_logits;
   aa.draft = draft_logits;
@@ -185,9 +194,9 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
   aa.K = K;
   aa.V = V;
   aa.tiles_per_row = (int)tiles_per_row(V, dtype);
-  aa.n_target_rows = (long long)B * (K + 1);
-  aa.nvec = nvec;
-  aa.vecs_per_cta = vpc;
+  aa.n_target_rows = B * (K + 1);
+  aa.ngroups = ngroups;
+  aa.groups_per_cta = gpc;
   aa.partials = (const float2*)((const char*)workspace + kHeaderBytes);
   aa.err = (unsigned*)workspace;
   aa.accepted_len = accepted_len;
@@ -200,7 +209,7 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3((unsigned)B * (unsigned)cs);
   cfg.blockDim = dim3(sv::kP2Threads);
-  cfg.dynamicSmemBytes = (size_t)vpc * sizeof(float4);
+  cfg.dynamicSmemBytes = accept_smem_bytes(gpc);
   cfg.stream = st;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
@@ -235,8 +244,8 @@ extern "C" {
 
 int spec_verify_max_vocab(int dtype) {
   if (dtype != SV_F32 && dtype != SV_BF16) return 0;
-  // every CTA of the cluster keeps 16 bytes of shared memory per vector it owns
-  return sv::kMaxClusterSize * sv::kMaxVecsPerCta * vec_of(dtype);
+  // every CTA of a 16-CTA cluster owns at most kMaxGroupsPerCta groups
+  return sv::kMaxClusterSize * kMaxGroupsPerCta * sv::kGroupVecs * vec_of(dtype);
 }
 
 size_t spec_verify_workspace_bytes(int B, int K, int V, int dtype) {

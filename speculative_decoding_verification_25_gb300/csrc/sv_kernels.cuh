@@ -1,16 +1,20 @@
 // The two kernels of spec_verify.
 //
-//   sv_row_stats_kernel  (the streaming pass) reads every logit row once,
-//     16 bytes per lane per load, and writes one partial per 4 KB tile:
-//     (tile max m, sum of e^((x - m)/T)) for rows of tempered rows, or
-//     (max logit, lowest index of it) for target rows of greedy rows.
-//     Draft rows of greedy rows are not read at all.
+//   Row statistics (the streaming pass) reads every logit row once.  Each
+//   warp streams a contiguous range of 2 KB row tiles (16 bytes per lane per
+//   load, the next tile in flight while the current one is reduced) and
+//   writes one partial per tile:
+//     tempered rows:  (MC, S) with S = sum of 2^(x*c - MC), c = log2(e)/T
+//                     rounded to float32 and MC a float32 shift >= max x*c;
+//     greedy rows:    (max logit, lowest index holding it).
+//   A lane folds its tiles into running values and the warp reduces them
+//   only where its range leaves a row; the other tiles of that stretch get
+//   the neutral partial (-inf, 0).  Draft rows of greedy rows are not read.
 //
-//   sv_accept_sample_kernel  (one thread-block cluster per batch row)
-//     folds the tile partials into row statistics, runs the left-to-right
-//     acceptance test, and draws the replacement or bonus token by inverse
-//     CDF over the one position that needs it, re-reading only that
-//     position's target (and draft) row.
+//   Accept + sample (one thread-block cluster per batch row) folds the
+//   partials into row statistics, runs the left-to-right acceptance test,
+//   and draws the replacement or bonus token by inverse CDF over the one
+//   position that needs it, re-reading only that position's rows.
 //
 // The rule is the exact rejection rule of the lesson "Decodificação
 // Especulativa e EAGLE" (ai-engineering.academy, phase 10 lesson 25),
@@ -28,13 +32,16 @@ namespace sv {
 namespace cg = cooperative_groups;
 
 constexpr int kMaxK = 16;
+constexpr int kTileVecsPerLane = 4;               // 4 x 16 B per lane
+constexpr int kTileVecs = 32 * kTileVecsPerLane;  // one 2 KB tile of one row
 constexpr int kP1Threads = 256;
-constexpr int kTileVecsPerLane = 8;             // 8 x 16 B = 128 B per lane
-constexpr int kTileVecs = 32 * kTileVecsPerLane; // 4 KB of one row per tile
-constexpr int kP2Threads = 512;
+
+constexpr int kP2Threads = 256;
 constexpr int kP2Warps = kP2Threads / 32;
-constexpr int kMaxClusterSize = 8;
-constexpr int kMaxVecsPerCta = 8192;            // 16 B of smem per vector -> 128 KB
+constexpr int kGroupVecs = 4;                     // a sampling group: 64 B of each row
+constexpr int kMaxGroupsPerThread = 8;
+constexpr int kMaxClusterSize = 16;
+constexpr int kQueueCap = 32;                     // large-term queue entries per warp
 // A term whose probability exceeds this is evaluated in double-float
 // during sampling; smaller terms use the float32 path.
 constexpr float kBigProb = 1.0e-4f;
@@ -51,14 +58,166 @@ struct RowStatsArgs {
   int B, K, V;
   int tiles_per_row;
   long long n_tiles;          // (B*(K+1) + B*K) * tiles_per_row
-  long long n_target_rows;    // B*(K+1)
+  int n_target_rows;          // B*(K+1)
   float2* partials;           // [n_target_rows + B*K][tiles_per_row]
   unsigned* err;
 };
 
+// float32 c = log2(e)/T, the same in both kernels
+__device__ __forceinline__ float log2e_over_f(float T) { return __fdiv_rn(kLog2eHi, T); }
+
+// Row `row` of the stacked [target rows; draft rows] and its batch row.
+__device__ __forceinline__ void row_info(const RowStatsArgs& a, int row, int& b, bool& is_draft,
+                                         int& r) {
+  is_draft = row >= a.n_target_rows;
+  r = is_draft ? row - a.n_target_rows : row;
+  b = is_draft ? r / a.K : r / (a.K + 1);
+}
+
 // ============================================================== streaming pass
+// One tile of one lane: kTileVecsPerLane 16-byte vectors, 512 bytes apart.
 template <typename E, bool kAligned>
-__global__ void __launch_bounds__(kP1Threads) sv_row_stats_kernel(RowStatsArgs a) {
+__device__ __forceinline__ void load_tile(uint32_t (&w)[kTileVecsPerLane][4], const char* rowp,
+                                          int ti, int lane, int V, bool full, bool act) {
+  if (!act) {
+#pragma unroll
+    for (int j = 0; j < kTileVecsPerLane; ++j) w[j][0] = w[j][1] = w[j][2] = w[j][3] = E::kFillWord;
+    return;
+  }
+  if (kAligned && full) {
+    // a whole tile inside the row: one base pointer, immediate offsets
+    const uint4* p = reinterpret_cast<const uint4*>(rowp) + (long long)ti * kTileVecs + lane;
+#pragma unroll
+    for (int j = 0; j < kTileVecsPerLane; ++j) ldg_stream16(p + 32 * j, w[j]);
+  } else {
+    const long long v0 = (long long)ti * kTileVecs + lane;
+#pragma unroll
+    for (int j = 0; j < kTileVecsPerLane; ++j) load_vec<E, kAligned>(rowp, v0 + 32 * j, V, w[j]);
+  }
+}
+
+// Running per-lane values of a row stretch.
+struct LaneStats {
+  float mc, s;       // tempered rows: shift (c-scaled) and sum of 2^(x c - mc)
+  float best;        // greedy rows: max logit ...
+  int bi;            // ... and its lowest index
+  __device__ __forceinline__ void reset() {
+    mc = SV_NEG_INF;
+    s = 0.f;
+    best = SV_NEG_INF;
+    bi = 0x7fffffff;
+  }
+};
+
+template <typename E>
+__device__ __forceinline__ void fold_tile(const uint32_t (&w)[kTileVecsPerLane][4], long long v0,
+                                          bool greedy, float c, LaneStats& st) {
+  if (greedy) {
+#pragma unroll
+    for (int j = 0; j < kTileVecsPerLane; ++j) {
+#pragma unroll
+      for (int k = 0; k < E::kVec; ++k) {
+        const float x = E::elem(w[j], k);
+        if (x > st.best) {
+          st.best = x;
+          st.bi = (int)((v0 + 32 * j) * E::kVec + k);
+        }
+      }
+    }
+    return;
+  }
+  // lane max of the tile, then one FFMA + ex2 + add per element
+  float m;
+  if constexpr (E::kBytes == 2) {
+    uint32_t mm = 0xff80ff80u;
+#pragma unroll
+    for (int j = 0; j < kTileVecsPerLane; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mm = bf2_max(mm, w[j][i]);
+    m = fmaxf(__uint_as_float(mm << 16), __uint_as_float(mm & 0xffff0000u));
+  } else {
+    m = SV_NEG_INF;
+#pragma unroll
+    for (int j = 0; j < kTileVecsPerLane; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m = fmaxf(m, __uint_as_float(w[j][i]));
+  }
+  if (m == SV_NEG_INF) return;
+  const float tmc = __fmul_rn(m, c);
+  if (tmc > st.mc) {   // new lane shift: rescale what was summed so far
+    st.s *= ex2_approx(__fsub_rn(st.mc, tmc));
+    st.mc = tmc;
+  }
+  const float nmc = -st.mc;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < kTileVecsPerLane; ++j) {
+#pragma unroll
+    for (int k = 0; k < E::kVec; k += 4) {
+      a0 += ex2_approx(__fmaf_rn(E::elem(w[j], k + 0), c, nmc));
+      a1 += ex2_approx(__fmaf_rn(E::elem(w[j], k + 1), c, nmc));
+      a2 += ex2_approx(__fmaf_rn(E::elem(w[j], k + 2), c, nmc));
+      a3 += ex2_approx(__fmaf_rn(E::elem(w[j], k + 3), c, nmc));
+    }
+  }
+  st.s += (a0 + a1) + (a2 + a3);
+}
+
+// Warp-combine the lane values of a finished row stretch [first, last] and
+// write its partials: the combined one at `last`, neutral ones before it.
+__device__ __forceinline__ void flush_stretch(float2* pp, int first, int last, bool greedy,
+                                              int lane, const LaneStats& st) {
+  float2 part;
+  if (greedy) {
+    const float m = warp_max(st.best);
+    const int idx = warp_min_int(st.best == m ? st.bi : 0x7fffffff);
+    part = make_float2(m, __int_as_float(idx));
+  } else {
+    const float M = warp_max(st.mc);
+    float sv = (st.mc == SV_NEG_INF) ? 0.f : st.s * ex2_approx(__fsub_rn(st.mc, M));
+    sv = warp_sum(sv);
+    part = make_float2(M, sv);
+  }
+  const float2 neutral = make_float2(SV_NEG_INF, greedy ? __int_as_float(0x7fffffff) : 0.f);
+  for (int k = first + lane; k <= last; k += 32) pp[k] = (k == last) ? part : neutral;
+}
+
+// Parameters of one row of the stacked [target rows; draft rows].
+struct RowParams {
+  bool active, greedy;
+  float c;
+  const char* rowp;
+  __device__ __forceinline__ RowParams(const RowStatsArgs& a, int row, int elem_bytes) {
+    int b, r;
+    bool is_draft;
+    row_info(a, row, b, is_draft, r);
+    const float T = __ldg(a.temperature + b);
+    greedy = (T == 0.f);
+    active = valid_temperature(T) && !(is_draft && greedy);
+    c = greedy ? 0.f : log2e_over_f(T);
+    rowp = (const char*)(is_draft ? a.draft : a.target) + (long long)r * a.V * elem_bytes;
+  }
+};
+
+// Fold tiles [ti0, ti1) of one row into `st`, two tiles per trip with the
+// next tile's loads in flight while the current one is folded.
+template <typename E, bool kAligned, bool kGreedy>
+__device__ __forceinline__ void fold_stretch(const RowParams& rp, int ti0, int ti1, int lane, int V,
+                                             int full_end, LaneStats& st) {
+  uint32_t wa[kTileVecsPerLane][4], wb[kTileVecsPerLane][4];
+  load_tile<E, kAligned>(wa, rp.rowp, ti0, lane, V, ti0 < full_end, true);
+  for (int ti = ti0; ti < ti1; ti += 2) {
+    const bool has1 = ti + 1 < ti1;
+    if (has1) load_tile<E, kAligned>(wb, rp.rowp, ti + 1, lane, V, ti + 1 < full_end, true);
+    fold_tile<E>(wa, (long long)ti * kTileVecs + lane, kGreedy, rp.c, st);
+    if (!has1) break;
+    if (ti + 2 < ti1) load_tile<E, kAligned>(wa, rp.rowp, ti + 2, lane, V, ti + 2 < full_end, true);
+    fold_tile<E>(wb, (long long)(ti + 1) * kTileVecs + lane, kGreedy, rp.c, st);
+  }
+}
+
+template <typename E, bool kAligned>
+__global__ void __launch_bounds__(kP1Threads, 4) sv_row_stats_kernel(RowStatsArgs a) {
   if (blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0u;
   // let the dependent accept/sample grid get scheduled early
   asm volatile("griddepcontrol.launch_dependents;");
@@ -68,69 +227,24 @@ __global__ void __launch_bounds__(kP1Threads) sv_row_stats_kernel(RowStatsArgs a
   const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
   const long long t0 = gw * a.n_tiles / nw;
   const long long t1 = (gw + 1) * a.n_tiles / nw;
-  if (t0 >= t1) return;
-  long long row = t0 / a.tiles_per_row;
-  int ti = (int)(t0 - row * a.tiles_per_row);
+  const int tpr = a.tiles_per_row;
+  // tiles below full_end lie wholly inside the row (the last one may be ragged)
+  const int full_end = ((long long)tpr * kTileVecs * E::kVec == a.V) ? tpr : tpr - 1;
 
-  for (long long tile = t0; tile < t1; ++tile) {
-    const bool is_draft = row >= a.n_target_rows;
-    const long long r = is_draft ? row - a.n_target_rows : row;
-    const int b = (int)(r / (is_draft ? a.K : a.K + 1));
-    const float T = __ldg(a.temperature + b);
-    const bool greedy = (T == 0.f);
-    if (valid_temperature(T) && !(is_draft && greedy)) {
-      const char* rowp =
-          (const char*)(is_draft ? a.draft : a.target) + r * (long long)a.V * E::kBytes;
-      const long long v0 = (long long)ti * kTileVecs + lane;
-      uint32_t w[kTileVecsPerLane][4];
-#pragma unroll
-      for (int j = 0; j < kTileVecsPerLane; ++j) load_vec<E, kAligned>(rowp, v0 + 32 * j, a.V, w[j]);
-
-      float2 part;
-      if (greedy) {
-        // max logit and the lowest index holding it
-        float best = SV_NEG_INF;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < kTileVecsPerLane; ++j) {
-#pragma unroll
-          for (int k = 0; k < E::kVec; ++k) {
-            const float x = E::elem(w[j], k);
-            if (x > best) {
-              best = x;
-              bi = (int)((v0 + 32 * j) * E::kVec + k);
-            }
-          }
-        }
-        const float m = warp_max(best);
-        const int idx = warp_min_int(best == m ? bi : 0x7fffffff);
-        part = make_float2(m, __int_as_float(idx));
-      } else {
-        float m = SV_NEG_INF;
-#pragma unroll
-        for (int j = 0; j < kTileVecsPerLane; ++j)
-#pragma unroll
-          for (int k = 0; k < E::kVec; ++k) m = fmaxf(m, E::elem(w[j], k));
-        m = warp_max(m);
-        float s = 0.f;
-        if (m != SV_NEG_INF) {
-          const float c = __fdiv_rn(kLog2eHi, T);
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int j = 0; j < kTileVecsPerLane; ++j)
-#pragma unroll
-            for (int k = 0; k < E::kVec; ++k)
-              acc[k & 3] += ex2_approx(__fmul_rn(__fsub_rn(E::elem(w[j], k), m), c));
-          s = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
-        }
-        part = make_float2(m, s);
-      }
-      if (lane == 0) a.partials[row * a.tiles_per_row + ti] = part;
+  // the warp's range crosses a few rows: one stretch per row
+  for (long long tile = t0; tile < t1;) {
+    const int row = (int)(tile / tpr);
+    const int ti0 = (int)(tile - (long long)row * tpr);
+    const int ti1 = (int)min((long long)tpr, ti0 + (t1 - tile));
+    const RowParams rp(a, row, E::kBytes);
+    if (rp.active) {
+      LaneStats st;
+      st.reset();
+      if (rp.greedy) fold_stretch<E, kAligned, true>(rp, ti0, ti1, lane, a.V, full_end, st);
+      else fold_stretch<E, kAligned, false>(rp, ti0, ti1, lane, a.V, full_end, st);
+      flush_stretch(a.partials + (long long)row * tpr, ti0, ti1 - 1, rp.greedy, lane, st);
     }
-    if (++ti == a.tiles_per_row) {
-      ti = 0;
-      ++row;
-    }
+    tile += ti1 - ti0;
   }
 }
 
@@ -143,9 +257,9 @@ struct AcceptArgs {
   const float* temperature;
   int B, K, V;
   int tiles_per_row;
-  long long n_target_rows;
-  int nvec;                   // vectors per logit row
-  int vecs_per_cta;           // vectors of one row owned by one CTA of the cluster
+  int n_target_rows;
+  int ngroups;                // sampling groups per logit row
+  int groups_per_cta;         // groups of one row owned by one CTA of the cluster
   const float2* partials;
   unsigned* err;
   int32_t* accepted_len;
@@ -160,7 +274,7 @@ struct CtaRecord {
   DF Q;            // sum of e^q over elements with positive weight
   DF Sp;           // sum of e^p over the slice
   DF Sq;           // sum of e^q over the slice
-  int last_vec;    // last vector (row-global index) with positive weight, -1 if none
+  int last_group;  // last group (row-global index) with positive weight, -1 if none
   int pad;
 };
 
@@ -169,204 +283,322 @@ struct Decision {
   int need_p_fallback;   // residual was zero everywhere: redo the sweep on p
   int rstar;             // CTA rank that locates the token
   int fallback_last;     // u*W fell beyond the total: take the last positive element
-  int last_vec;
+  int last_group;
   DF tau_local;          // target mass inside CTA rstar
   DF dc;                 // c_true - c_used
 };
 
-struct SampleSmem {
+struct AcceptSmem {
   float2 tab[256];
-  DF warpW[kP2Warps], warpQ[kP2Warps], warpP[kP2Warps], warpSq[kP2Warps];
-  int warpLast[kP2Warps];
-  CtaRecord rec;
-  Decision dec;
-  float rowM[2 * kMaxK + 1];
+  float rowMC[2 * kMaxK + 1];
   float rowS[2 * kMaxK + 1];
   int rowArg[kMaxK + 1];
-  int n;
+  int tok[kMaxK];
+  float r[kMaxK + 1];
+  float xp[kMaxK];
+  float xq[kMaxK];
   int bad;
-  int lane_pick;
-  int vec_pick;
-  DF tau_vec;
+  int n;
+  DF red[kP2Warps][4];
+  int redi[kP2Warps];
+  CtaRecord rec;
+  CtaRecord recs[kMaxClusterSize];
+  Decision dec;
+  int pick_thread;
+  int pick_last;
+  int group_pick;
+  DF tau_group;
+  DF warp_tot[kP2Warps];
+  // large terms: per-lane raw words of the current group (staged only by
+  // lanes that have one), the warp's queue of terms and their results
+  uint4 raw[kP2Warps][32][2 * kGroupVecs];
+  float2 qx[kP2Warps][kQueueCap];
+  float4 qres[kP2Warps][kQueueCap];
+  DF red1[4];
 };
 
-// Weight of element k of a loaded vector pair, exactly as the sweep counts it.
-// kResidual: w = max(e^p - c e^q, 0) and the e^q that goes with it when w > 0;
-// otherwise w = e^p.  Elements whose probability is above kBigProb are
-// evaluated in double-float, the rest in float32.
-template <typename E, bool kResidual>
-__device__ __forceinline__ void eval_elem(const uint32_t (&wp)[4], const uint32_t (&wq)[4], int k,
-                                          float Mp, float Mq, DF L, float c, float thp,
-                                          float thq, const float2* tab, DF& w, DF& q) {
-  const float xp = E::elem(wp, k);
-  const float ep = ex2_approx(__fmul_rn(__fsub_rn(xp, Mp), L.hi));
+// Everything the sampling sweep needs about the sampled position.
+struct SampleCtx {
+  const char* rowP;
+  const char* rowQ;
+  int V, g0, ng;          // CTA groups [g0, g0 + ng)
+  float MCp, MCq;         // shifts (c-scaled) of the two rows
+  float c_hi, c_lo;       // log2(e)/T as hi + lo
+  float cw;               // c_used = S_p / S_q at the pass-1 shifts
+  float thp, thq;         // big-term thresholds on 2^(x c - MC)
+  DF L;                   // log2(e)/T as a double-float (= c_hi + c_lo)
+};
+
+// e = 2^(x * L - MC) for the float32 path: the product and the shift are
+// formed exactly by the FMA and rounded once, plus the low part of L.
+// c_lo > 0 (see SampleCtx), so x = -inf gives -inf, not inf - inf.
+__device__ __forceinline__ float small_exp(float x, float MC, const SampleCtx& s) {
+  return ex2_approx(__fmaf_rn(x, s.c_lo, __fmaf_rn(x, s.c_hi, -MC)));
+}
+// the same value in double-float: 2^(x*L - MC) with x*L exact (two-product)
+__device__ __forceinline__ DF big_exp(float x, float MC, const SampleCtx& s, const float2* tab) {
+  const float ph = __fmul_rn(x, s.L.hi);
+  float pl = __fmaf_rn(x, s.L.hi, -ph);
+  pl = __fmaf_rn(x, s.L.lo, pl);
+  const DF y = df_add(DF{ph, pl}, DF{-MC, 0.f});
+  return exp2_df(y.hi, y.lo, tab);
+}
+
+// Weight of element xp (and xq) as the sweep counts it.  kResidual:
+// w = max(e^p - cw e^q, 0) with the e^q that goes with a positive w;
+// otherwise w = e^p.  Large terms in double-float, the rest in float32.
+template <bool kResidual>
+__device__ __forceinline__ void eval_pair(float xp, float xq, const SampleCtx& s, const float2* tab,
+                                          DF& w, DF& q) {
+  const float ep = small_exp(xp, s.MCp, s);
   if (kResidual) {
-    const float xq = E::elem(wq, k);
-    const float eq = ex2_approx(__fmul_rn(__fsub_rn(xq, Mq), L.hi));
-    if (ep > thp || eq > thq) {
-      const DF epd = exp_df(xp, Mp, L, tab);
-      const DF eqd = exp_df(xq, Mq, L, tab);
-      const DF d = df_sub(epd, df_mul_f(eqd, c));
-      if (df_pos(d)) {
-        w = d;
-        q = eqd;
-      } else {
-        w = DF{0.f, 0.f};
-        q = DF{0.f, 0.f};
-      }
+    const float eq = small_exp(xq, s.MCq, s);
+    if (ep > s.thp || eq > s.thq) {
+      const DF epd = big_exp(xp, s.MCp, s, tab);
+      const DF eqd = big_exp(xq, s.MCq, s, tab);
+      const DF d = df_sub(epd, df_mul_f(eqd, s.cw));
+      w = df_pos(d) ? d : DF{0.f, 0.f};
+      q = df_pos(d) ? eqd : DF{0.f, 0.f};
     } else {
-      const float d = __fmaf_rn(-c, eq, ep);
+      const float d = __fmaf_rn(-s.cw, eq, ep);
       w = DF{d > 0.f ? d : 0.f, 0.f};
       q = DF{d > 0.f ? eq : 0.f, 0.f};
     }
   } else {
-    if (ep > thp) {
-      w = exp_df(xp, Mp, L, tab);
-    } else {
-      w = DF{ep, 0.f};
-    }
+    w = (ep > s.thp) ? big_exp(xp, s.MCp, s, tab) : DF{ep, 0.f};
     q = DF{0.f, 0.f};
   }
 }
 
-// Sweep of one CTA over its slice of the row(s): per-vector weight sums go
-// to s_vec, per-warp totals to sm.warp*, the CTA total to sm.rec.
-template <typename E, bool kAligned, bool kResidual>
-__device__ void sweep_slice(const char* rowP, const char* rowQ, int V, int cv0, int ncv, float Mp,
-                            float Mq, DF L, float c, float thp, float thq, SampleSmem& sm,
-                            float4* s_vec) {
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int nwr = (ncv + 31) >> 5;
-  const int wr0 = warp * nwr / kP2Warps, wr1 = (warp + 1) * nwr / kP2Warps;
-  DF accW{0.f, 0.f}, accQ{0.f, 0.f}, accP{0.f, 0.f}, accSq{0.f, 0.f};
-  int last = -1;
-  for (int wr = wr0; wr < wr1; ++wr) {
-    const int vl = wr * 32 + lane;
-    const bool valid = vl < ncv;
-    const long long v = (long long)cv0 + vl;
-    uint32_t wp[4], wq[4];
-    if (valid) {
-      load_vec<E, kAligned>(rowP, v, V, wp);
-      if (kResidual) load_vec<E, kAligned>(rowQ, v, V, wq);
-    } else {
-      wp[0] = wp[1] = wp[2] = wp[3] = E::kFillWord;
+// Block-wide sum of four double-floats; every thread gets the totals.
+__device__ __forceinline__ void block_sum4(DF (&v)[4], AcceptSmem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = warp_sum_df(v[i]);
+  if (lane == 0)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sm.red[warp][i] = v[i];
+  __syncthreads();
+  if (threadIdx.x < 4) {
+    DF t{0.f, 0.f};
+    for (int w = 0; w < kP2Warps; ++w) t = df_add(t, sm.red[w][threadIdx.x]);
+    sm.red1[threadIdx.x] = t;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = sm.red1[i];
+}
+
+__device__ __forceinline__ int block_max_int(int v, AcceptSmem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (lane == 0) sm.redi[warp] = v;
+  __syncthreads();
+  int t = sm.redi[0];
+  for (int w = 1; w < kP2Warps; ++w) t = max(t, sm.redi[w]);
+  __syncthreads();
+  return t;
+}
+
+// Load group g (kGroupVecs vectors) of a row.
+template <typename E, bool kAligned>
+__device__ __forceinline__ void load_group(const char* row, int g, int V, uint32_t (&w)[kGroupVecs][4]) {
+#pragma unroll
+  for (int j = 0; j < kGroupVecs; ++j) load_vec<E, kAligned>(row, (long long)g * kGroupVecs + j, V, w[j]);
+}
+
+// The large terms of one group step, in double-float.  Every lane with a
+// set bit in `big` has staged its group's raw words in sm.raw[warp][lane];
+// the warp lays all terms out in one queue (lane order), evaluates up to
+// kQueueCap at a time, one per lane, and each lane folds back its own
+// contiguous slice of results into (wg, qg) and the totals (accP, accQ).
+template <typename E, bool kResidual>
+__device__ __noinline__ void large_terms(const SampleCtx& x, AcceptSmem& sm, int warp, int lane,
+                                         unsigned big, DF* sums) {
+  const int cnt = __popc(big);
+  int off = cnt;   // inclusive scan of the counts
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, off, o);
+    if (lane >= o) off += v;
+  }
+  const int total = __shfl_sync(0xffffffffu, off, 31);
+  off -= cnt;
+  DF wg = sums[0], qg = sums[1], accP = sums[2], accQ = sums[3];
+  const uint32_t* rawp = reinterpret_cast<const uint32_t*>(sm.raw[warp][lane]);
+  for (int base = 0; base < total; base += kQueueCap) {
+    // lay out this window of the queue
+    {
+      unsigned m = big;
+      int idx = off;
+      while (m) {
+        const int e = __ffs(m) - 1;
+        m &= m - 1u;
+        if (idx >= base && idx < base + kQueueCap) {
+          const int j = e / E::kVec, k = e % E::kVec;
+          const uint32_t wpk[4] = {rawp[4 * j], rawp[4 * j + 1], rawp[4 * j + 2], rawp[4 * j + 3]};
+          float xq = 0.f;
+          if (kResidual) {
+            const int jq = kGroupVecs + j;
+            const uint32_t wqk[4] = {rawp[4 * jq], rawp[4 * jq + 1], rawp[4 * jq + 2], rawp[4 * jq + 3]};
+            xq = E::elem(wqk, k);
+          }
+          sm.qx[warp][idx - base] = make_float2(E::elem(wpk, k), xq);
+        }
+        ++idx;
+      }
     }
-    if (!kResidual || !valid) wq[0] = wq[1] = wq[2] = wq[3] = E::kFillWord;
+    __syncwarp();
+    const int n = min(kQueueCap, total - base);
+    for (int i = lane; i < n; i += 32) {
+      const float2 xx = sm.qx[warp][i];
+      const DF epd = big_exp(xx.x, x.MCp, x, sm.tab);
+      DF w = epd, q{0.f, 0.f}, Q{0.f, 0.f};
+      if (kResidual) {
+        Q = big_exp(xx.y, x.MCq, x, sm.tab);
+        const DF d = df_sub(epd, df_mul_f(Q, x.cw));
+        w = df_pos(d) ? d : DF{0.f, 0.f};
+        q = df_pos(d) ? Q : DF{0.f, 0.f};
+      }
+      sm.qres[warp][i] = make_float4(w.hi, w.lo, q.hi, q.lo);
+      // the totals do not care which lane adds them
+      accP = df_add(accP, epd);
+      if (kResidual) accQ = df_add(accQ, Q);
+    }
+    __syncwarp();
+    for (int i = max(off, base); i < min(off + cnt, base + n); ++i) {
+      const float4 r = sm.qres[warp][i - base];
+      wg = df_add(wg, DF{r.x, r.y});
+      qg = df_add(qg, DF{r.z, r.w});
+    }
+    __syncwarp();
+  }
+  sums[0] = wg;
+  sums[1] = qg;
+  sums[2] = accP;
+  sums[3] = accQ;
+}
+
+// One sweep of this CTA over its groups of the sampled row(s).  Per-group
+// weights go to part[] (w.hi, w.lo, q.hi, q.lo); the CTA record to sm.rec.
+// The per-thread sums of part[] over the thread's contiguous run of groups
+// come back in Wt, Qt (the locate step scans them).
+template <typename E, bool kAligned, bool kResidual>
+__device__ void sweep_slice(const SampleCtx& x, AcceptSmem& sm, float4* part, DF& Wt, DF& Qt) {
+  const int tid = threadIdx.x;
+  DF accP{0.f, 0.f}, accQ{0.f, 0.f};
+  int lastg = -1;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int iters = (x.ng + kP2Threads - 1) / kP2Threads;   // the same for every thread
+  for (int it = 0; it < iters; ++it) {
+    const int gl = it * kP2Threads + tid;
+    const bool valid = gl < x.ng;
+    const int g = x.g0 + gl;
+    uint32_t wp[kGroupVecs][4], wq[kGroupVecs][4];
+#pragma unroll
+    for (int j = 0; j < kGroupVecs; ++j) {
+      wp[j][0] = wp[j][1] = wp[j][2] = wp[j][3] = E::kFillWord;
+      wq[j][0] = wq[j][1] = wq[j][2] = wq[j][3] = E::kFillWord;
+    }
+    if (valid) {
+      load_group<E, kAligned>(x.rowP, g, x.V, wp);
+      if (kResidual) load_group<E, kAligned>(x.rowQ, g, x.V, wq);
+    }
+    // float32 pass; large terms only leave a bit in `big`
     float sw = 0.f, sq = 0.f, sp = 0.f, sQ = 0.f;
     unsigned big = 0u;
 #pragma unroll
-    for (int k = 0; k < E::kVec; ++k) {
-      const float ep = ex2_approx(__fmul_rn(__fsub_rn(E::elem(wp, k), Mp), L.hi));
-      if (kResidual) {
-        const float eq = ex2_approx(__fmul_rn(__fsub_rn(E::elem(wq, k), Mq), L.hi));
-        if (ep > thp || eq > thq) {
-          big |= 1u << k;
-        } else {
-          const float d = __fmaf_rn(-c, eq, ep);
-          sw += d > 0.f ? d : 0.f;
-          sq += d > 0.f ? eq : 0.f;
-          sp += ep;
-          sQ += eq;
-        }
-      } else {
-        if (ep > thp) {
-          big |= 1u << k;
-        } else {
-          sw += ep;
-          sp += ep;
-        }
-      }
-    }
-    DF wb{0.f, 0.f}, qb{0.f, 0.f}, pb{0.f, 0.f}, Qb{0.f, 0.f};
-    // the rare large terms, in double-float; every lane with one pending
-    // works on it in the same pass
-    while (__any_sync(0xffffffffu, big != 0u)) {
-      if (big) {
-        const int k = __ffs(big) - 1;
-        big &= big - 1u;
-        const float xp = E::elem(wp, k);
-        const DF epd = exp_df(xp, Mp, L, sm.tab);
-        pb = df_add(pb, epd);
-        if (kResidual) {
-          const DF eqd = exp_df(E::elem(wq, k), Mq, L, sm.tab);
-          Qb = df_add(Qb, eqd);
-          const DF d = df_sub(epd, df_mul_f(eqd, c));
-          if (df_pos(d)) {
-            wb = df_add(wb, d);
-            qb = df_add(qb, eqd);
-          }
-        } else {
-          wb = df_add(wb, epd);
-        }
-      }
-    }
-    const DF wv = df_add_f(wb, sw);
-    const DF qv = df_add_f(qb, sq);
-    if (valid) {
-      s_vec[vl] = make_float4(wv.hi, wv.lo, qv.hi, qv.lo);
-      if (df_pos(wv)) last = (int)v;
-    }
-    accW = df_add(accW, wv);
-    accQ = df_add(accQ, qv);
-    accP = df_add(accP, df_add_f(pb, sp));
-    accSq = df_add(accSq, df_add_f(Qb, sQ));
-  }
-  accW = warp_sum_df(accW);
-  accQ = warp_sum_df(accQ);
-  accP = warp_sum_df(accP);
-  accSq = warp_sum_df(accSq);
+    for (int j = 0; j < kGroupVecs; ++j) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-  if (lane == 0) {
-    sm.warpW[warp] = accW;
-    sm.warpQ[warp] = accQ;
-    sm.warpP[warp] = accP;
-    sm.warpSq[warp] = accSq;
-    sm.warpLast[warp] = last;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    CtaRecord rec;
-    rec.W = rec.Q = rec.Sp = rec.Sq = DF{0.f, 0.f};
-    rec.last_vec = -1;
-    rec.pad = 0;
-    for (int i = 0; i < kP2Warps; ++i) {
-      rec.W = df_add(rec.W, sm.warpW[i]);
-      rec.Q = df_add(rec.Q, sm.warpQ[i]);
-      rec.Sp = df_add(rec.Sp, sm.warpP[i]);
-      rec.Sq = df_add(rec.Sq, sm.warpSq[i]);
-      rec.last_vec = max(rec.last_vec, sm.warpLast[i]);
+      for (int k = 0; k < E::kVec; ++k) {
+        const float ep = small_exp(E::elem(wp[j], k), x.MCp, x);
+        if (kResidual) {
+          const float eq = small_exp(E::elem(wq[j], k), x.MCq, x);
+          const bool b = ep > x.thp || eq > x.thq;
+          big |= (unsigned)b << (j * E::kVec + k);
+          const float d = b ? 0.f : __fmaf_rn(-x.cw, eq, ep);
+          sw += fmaxf(d, 0.f);
+          sq += d > 0.f ? eq : 0.f;
+          sp += b ? 0.f : ep;
+          sQ += b ? 0.f : eq;
+        } else {
+          const bool b = ep > x.thp;
+          big |= (unsigned)b << (j * E::kVec + k);
+          sw += b ? 0.f : ep;
+        }
+      }
     }
-    sm.rec = rec;
+    DF sums[4] = {DF{0.f, 0.f}, DF{0.f, 0.f}, accP, accQ};
+    if (__any_sync(0xffffffffu, big != 0u)) {
+      if (big) {
+#pragma unroll
+        for (int j = 0; j < kGroupVecs; ++j) {
+          sm.raw[warp][lane][j] = make_uint4(wp[j][0], wp[j][1], wp[j][2], wp[j][3]);
+          if (kResidual) sm.raw[warp][lane][kGroupVecs + j] = make_uint4(wq[j][0], wq[j][1], wq[j][2], wq[j][3]);
+        }
+      }
+      __syncwarp();
+      large_terms<E, kResidual>(x, sm, warp, lane, big, sums);
+    }
+    if (!kResidual) sp = sw;
+    const DF wg = df_add_f(sums[0], sw);
+    const DF qg = df_add_f(sums[1], sq);
+    if (valid) {
+      part[gl] = make_float4(wg.hi, wg.lo, qg.hi, qg.lo);
+      if (df_pos(wg)) lastg = g;
+    }
+    accP = df_add_f(sums[2], sp);
+    accQ = df_add_f(sums[3], sQ);
+  }
+  __syncthreads();   // part[] complete
+
+  // per-thread sums over a contiguous run of groups: the prefix structure
+  const int cpt = (x.ng + kP2Threads - 1) / kP2Threads;
+  const int a0 = min(x.ng, tid * cpt), a1 = min(x.ng, a0 + cpt);
+  DF W{0.f, 0.f}, Q{0.f, 0.f};
+  for (int gl = a0; gl < a1; ++gl) {
+    const float4 p4 = part[gl];
+    W = df_add(W, DF{p4.x, p4.y});
+    Q = df_add(Q, DF{p4.z, p4.w});
+  }
+  Wt = W;
+  Qt = Q;
+  DF tot[4] = {W, Q, accP, accQ};
+  block_sum4(tot, sm);
+  const int last = block_max_int(lastg, sm);
+  if (tid == 0) {
+    sm.rec.W = tot[0];
+    sm.rec.Q = tot[1];
+    sm.rec.Sp = tot[2];
+    sm.rec.Sq = tot[3];
+    sm.rec.last_group = last;
+    sm.rec.pad = 0;
   }
 }
 
-// Thread 0 of every CTA: combine the cluster's records into the decision.
-// Every CTA reads the same records in the same order, so all agree.
-__device__ void decide(cg::cluster_group& cluster, int cs, bool residual, float c_used, float u,
-                       int vecs_per_cta, SampleSmem& sm) {
-  DF Sp{0.f, 0.f}, Sq{0.f, 0.f};
-  CtaRecord recs[kMaxClusterSize];
+// Thread 0 of every CTA: combine the cluster's records (already copied
+// into recs[] by threads 0..cs-1) into the decision.  Every CTA reads the
+// same records in the same order, so all agree.
+__device__ void decide(const CtaRecord* recs, int cs, bool residual, float cw, float u,
+                       int groups_per_cta, AcceptSmem& sm) {
+  DF Sp{0.f, 0.f}, Sq{0.f, 0.f}, tot{0.f, 0.f};
+  int last_group = -1;
   for (int r = 0; r < cs; ++r) {
-    const CtaRecord* rp = cluster.map_shared_rank(&sm.rec, r);
-    recs[r] = *rp;
     Sp = df_add(Sp, recs[r].Sp);
     Sq = df_add(Sq, recs[r].Sq);
+    last_group = max(last_group, recs[r].last_group);
   }
   DF dc{0.f, 0.f};
-  if (residual) dc = df_sub(df_div(Sp, Sq), DF{c_used, 0.f});
-  DF Wc[kMaxClusterSize];
-  DF tot{0.f, 0.f};
-  int last_vec = -1;
+  if (residual) dc = df_sub(df_div(Sp, Sq), DF{cw, 0.f});
+  DF wr[kMaxClusterSize];
   for (int r = 0; r < cs; ++r) {
-    Wc[r] = residual ? df_sub(recs[r].W, df_mul(dc, recs[r].Q)) : recs[r].W;
-    tot = df_add(tot, Wc[r]);
-    last_vec = max(last_vec, recs[r].last_vec);
+    wr[r] = residual ? df_sub(recs[r].W, df_mul(dc, recs[r].Q)) : recs[r].W;
+    tot = df_add(tot, wr[r]);
   }
   Decision d;
   d.dc = dc;
-  d.last_vec = last_vec;
+  d.last_group = last_group;
   d.need_p_fallback = residual && !df_pos(tot);
   d.fallback_last = 0;
   d.rstar = -1;
@@ -376,8 +608,8 @@ __device__ void decide(cg::cluster_group& cluster, int cs, bool residual, float 
     const DF tau = df_mul_f(tot, u);
     DF pre{0.f, 0.f};
     for (int r = 0; r < cs; ++r) {
-      const DF nxt = df_add(pre, Wc[r]);
-      if (df_pos(Wc[r]) && df_lt(tau, nxt)) {
+      const DF nxt = df_add(pre, wr[r]);
+      if (df_pos(wr[r]) && df_lt(tau, nxt)) {
         d.rstar = r;
         d.tau_local = df_sub(tau, pre);
         break;
@@ -386,338 +618,340 @@ __device__ void decide(cg::cluster_group& cluster, int cs, bool residual, float 
     }
     if (d.rstar < 0) {
       d.fallback_last = 1;
-      d.rstar = last_vec >= 0 ? last_vec / vecs_per_cta : 0;
+      d.rstar = last_group >= 0 ? last_group / groups_per_cta : 0;
     }
   }
   sm.dec = d;
 }
 
-// Find the token inside CTA rstar.  Runs on all threads of that CTA.
-template <typename E, bool kAligned, bool kResidual>
-__device__ int locate(const char* rowP, const char* rowQ, int V, int cv0, int ncv, float Mp,
-                      float Mq, DF L, float c, float thp, float thq, SampleSmem& sm,
-                      const float4* s_vec) {
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
+// Find the token inside CTA rstar (all threads of that CTA).
+template <typename E, bool kResidual>
+__device__ int locate(const SampleCtx& x, AcceptSmem& sm, const float4* part, DF Wt, DF Qt) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const DF dc = sm.dec.dc;
-  const int nwr = (ncv + 31) >> 5;
-  int vstar = -1;            // CTA-local vector that holds the token
-  DF tau_v{0.f, 0.f};
-  bool last_mode = sm.dec.fallback_last != 0;
-  if (last_mode) {
-    vstar = sm.dec.last_vec - cv0;
-  } else {
-    // the warp, then the lane chunk, then the vector whose prefix passes tau
-    __shared__ int s_wstar;
-    __shared__ DF s_tauw;
-    if (threadIdx.x == 0) {
-      DF pre{0.f, 0.f};
-      int ws = -1, wlast = -1;
-      DF tw{0.f, 0.f};
-      for (int i = 0; i < kP2Warps; ++i) {
-        const DF wc = kResidual ? df_sub(sm.warpW[i], df_mul(dc, sm.warpQ[i])) : sm.warpW[i];
-        const DF nxt = df_add(pre, wc);
-        if (df_pos(wc)) {
-          wlast = i;
-          if (ws < 0 && df_lt(sm.dec.tau_local, nxt)) {
-            ws = i;
-            tw = df_sub(sm.dec.tau_local, pre);
-          }
-        }
-        pre = nxt;
-      }
-      if (ws < 0) {   // rounding pushed tau past this CTA's mass: last positive warp, top end
-        ws = wlast < 0 ? 0 : wlast;
-        tw = DF{3.4e38f, 0.f};
-      }
-      s_wstar = ws;
-      s_tauw = tw;
-    }
-    __syncthreads();
-    if (warp == s_wstar) {
-      const int vs = (warp * nwr / kP2Warps) * 32;
-      const int ve = min(ncv, ((warp + 1) * nwr / kP2Warps) * 32);
-      const int nv = max(0, ve - vs);
-      const int chunk = (nv + 31) >> 5;
-      const int a0 = vs + lane * chunk;
-      const int a1 = min(ve, a0 + chunk);
-      DF own{0.f, 0.f};
-      for (int i = a0; i < a1; ++i) {
-        const float4 s = s_vec[i];
-        DF wc{s.x, s.y};
-        if (kResidual) wc = df_sub(wc, df_mul(dc, DF{s.z, s.w}));
-        own = df_add(own, wc);
-      }
-      // inclusive scan over lanes
-      DF inc = own;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const DF up = df_shfl_up(inc, o);
-        if (lane >= o) inc = df_add(inc, up);
-      }
-      const DF exc = df_sub(inc, own);
-      const DF tw = s_tauw;
-      const bool hit = df_pos(own) && df_lt(tw, inc);
-      const unsigned hits = __ballot_sync(0xffffffffu, hit);
-      const unsigned posl = __ballot_sync(0xffffffffu, df_pos(own));
-      int lstar;
-      bool at_top = false;
-      if (hits) {
-        lstar = __ffs(hits) - 1;
-      } else {
-        lstar = posl ? 31 - __clz(posl) : 0;
-        at_top = true;
-      }
-      if (lane == lstar) {
-        DF run = exc;
-        int vs2 = -1, vlastpos = -1;
-        DF tv{0.f, 0.f};
-        for (int i = a0; i < a1; ++i) {
-          const float4 s = s_vec[i];
-          DF wc{s.x, s.y};
-          if (kResidual) wc = df_sub(wc, df_mul(dc, DF{s.z, s.w}));
-          const DF nxt = df_add(run, wc);
-          if (df_pos(wc)) {
-            vlastpos = i;
-            if (!at_top && vs2 < 0 && df_lt(tw, nxt)) {
-              vs2 = i;
-              tv = df_sub(tw, run);
-            }
-          }
-          run = nxt;
-        }
-        if (vs2 < 0) {   // fell off the end by rounding: top of the last positive vector
-          vs2 = vlastpos < 0 ? max(a0, 0) : vlastpos;
-          tv = DF{3.4e38f, 0.f};
-        }
-        sm.vec_pick = vs2;
-        sm.tau_vec = tv;
-      }
-      __syncwarp();
-    }
-    __syncthreads();
-    vstar = sm.vec_pick;
-    tau_v = sm.tau_vec;
-    if (tau_v.hi >= 3.4e38f) last_mode = true;
+  const DF huge{3.0e38f, 0.f};
+  const int cpt = (x.ng + kP2Threads - 1) / kP2Threads;
+  if (tid == 0) {
+    sm.pick_thread = 0x7fffffff;
+    sm.pick_last = -1;
   }
-  // walk the elements of vector vstar
+  bool last_mode = sm.dec.fallback_last != 0;
+  int gstar;
+  DF tau_g = huge;
+  if (last_mode) {
+    gstar = sm.dec.last_group - x.g0;
+  } else {
+    // exclusive / inclusive prefix of the corrected per-thread sums
+    const DF own = kResidual ? df_sub(Wt, df_mul(dc, Qt)) : Wt;
+    DF inc = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const DF up = df_shfl_up(inc, o);
+      if (lane >= o) inc = df_add(inc, up);
+    }
+    if (lane == 31) sm.warp_tot[warp] = inc;
+    __syncthreads();
+    DF wpre{0.f, 0.f};
+    for (int w = 0; w < warp; ++w) wpre = df_add(wpre, sm.warp_tot[w]);
+    DF exc = df_shfl_up(inc, 1);
+    if (lane == 0) exc = DF{0.f, 0.f};
+    exc = df_add(wpre, exc);
+    inc = df_add(wpre, inc);
+    const DF tau = sm.dec.tau_local;
+    if (df_pos(own)) {
+      if (df_lt(tau, inc)) atomicMin(&sm.pick_thread, tid);
+      atomicMax(&sm.pick_last, tid);
+    }
+    __syncthreads();
+    int ts = sm.pick_thread;
+    bool at_top = false;
+    if (ts == 0x7fffffff) {   // rounding pushed tau past this CTA's mass
+      ts = max(sm.pick_last, 0);
+      at_top = true;
+    }
+    if (tid == ts) {
+      DF run = exc;
+      int gs = -1, glast = -1;
+      DF tg = huge;
+      const int a0 = min(x.ng, tid * cpt), a1 = min(x.ng, a0 + cpt);
+      for (int gl = a0; gl < a1; ++gl) {
+        const float4 p4 = part[gl];
+        DF wc{p4.x, p4.y};
+        if (kResidual) wc = df_sub(wc, df_mul(dc, DF{p4.z, p4.w}));
+        const DF nxt = df_add(run, wc);
+        if (df_pos(wc)) {
+          glast = gl;
+          if (!at_top && gs < 0 && df_lt(tau, nxt)) {
+            gs = gl;
+            tg = df_sub(tau, run);
+          }
+        }
+        run = nxt;
+      }
+      if (gs < 0) {   // fell off the end by rounding: top of the last positive group
+        gs = glast >= 0 ? glast : a0;
+        tg = huge;
+      }
+      sm.group_pick = gs;
+      sm.tau_group = tg;
+    }
+    __syncthreads();
+    gstar = sm.group_pick;
+    tau_g = sm.tau_group;
+    if (tau_g.hi >= huge.hi) last_mode = true;
+  }
+  // the element inside group gstar: one lane per element, double-float scan
   int token = -1;
-  if (threadIdx.x == 0) {
-    const long long v = (long long)cv0 + max(vstar, 0);
-    uint32_t wp[4], wq[4];
-    load_vec<E, kAligned>(rowP, v, V, wp);
-    if (kResidual) {
-      load_vec<E, kAligned>(rowQ, v, V, wq);
-    } else {
-      wq[0] = wq[1] = wq[2] = wq[3] = E::kFillWord;
-    }
-    DF run{0.f, 0.f};
-    int lastpos = -1, best = -1;
-    float bestw = -1.f;
-    for (int k = 0; k < E::kVec; ++k) {
-      if (v * E::kVec + k >= V) break;
-      DF w, q;
-      eval_elem<E, kResidual>(wp, wq, k, Mp, Mq, L, c, thp, thq, sm.tab, w, q);
+  if (warp == 0) {
+    constexpr int kGroupElems = kGroupVecs * E::kVec;   // 32 (bf16) or 16 (f32)
+    const long long e = ((long long)x.g0 + max(gstar, 0)) * kGroupElems + lane;
+    const bool in = lane < kGroupElems && e < x.V;
+    DF w{0.f, 0.f}, q{0.f, 0.f};
+    if (in) {
+      const float xp = E::load_scalar(x.rowP, e);
+      const float xq = kResidual ? E::load_scalar(x.rowQ, e) : 0.f;
+      eval_pair<kResidual>(xp, xq, x, sm.tab, w, q);
       if (kResidual) w = df_sub(w, df_mul(dc, q));
-      if (w.hi > bestw) {
-        bestw = w.hi;
-        best = k;
-      }
-      if (!df_pos(w)) continue;
-      lastpos = k;
-      run = df_add(run, w);
-      if (!last_mode && df_lt(tau_v, run)) {
-        token = (int)(v * E::kVec + k);
-        break;
-      }
     }
-    if (token < 0) token = (int)(v * E::kVec + (lastpos >= 0 ? lastpos : max(best, 0)));
+    const bool pos = in && df_pos(w);
+    DF inc = pos ? w : DF{0.f, 0.f};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const DF up = df_shfl_up(inc, o);
+      if (lane >= o) inc = df_add(inc, up);
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, pos && !last_mode && df_lt(tau_g, inc));
+    const unsigned posm = __ballot_sync(0xffffffffu, pos);
+    int k;
+    if (hit) {
+      k = __ffs(hit) - 1;
+    } else if (posm) {
+      k = 31 - __clz(posm);
+    } else {
+      // nothing positive here (rounding): the largest weight of the group
+      float bw = in ? w.hi : -3.0e38f;
+      int bk = lane;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ow = __shfl_xor_sync(0xffffffffu, bw, o);
+        const int ok = __shfl_xor_sync(0xffffffffu, bk, o);
+        if (ow > bw || (ow == bw && ok < bk)) {
+          bw = ow;
+          bk = ok;
+        }
+      }
+      k = bk < kGroupElems ? bk : 0;
+    }
+    token = (int)(((long long)x.g0 + max(gstar, 0)) * kGroupElems + k);
   }
   return token;
 }
 
 template <typename E, bool kAligned>
-__global__ void __launch_bounds__(kP2Threads) sv_accept_sample_kernel(AcceptArgs a) {
-  extern __shared__ float4 s_vec[];
-  __shared__ SampleSmem sm;
+__global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptArgs a) {
+  extern __shared__ __align__(16) float4 s_part[];
+  __shared__ AcceptSmem sm;
   cg::cluster_group cluster = cg::this_cluster();
   const int cs = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
   const int b = blockIdx.x / cs;
   const int K = a.K;
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long ob = (long long)b * (K + 1);
 
-  // wait for the streaming pass (and the visibility of its writes)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
+  // ---------------- prologue: inputs only, overlaps the streaming pass
   const float T = __ldg(a.temperature + b);
   const bool greedy = (T == 0.f);
-  if (threadIdx.x == 0) {
-    int bad = valid_temperature(T) ? 0 : (int)kDevBadTemperature;
-    for (int t = 0; t < K && !bad; ++t) {
-      const int x = __ldg(a.tokens + (long long)b * K + t);
-      if (x < 0 || x >= a.V) bad = (int)kDevBadToken;
+  if (rank != 0 && (greedy || !valid_temperature(T))) return;   // rank 0 alone handles these
+  if (warp == 0) {
+    int x = 0;
+    bool tok_ok = true;
+    if (lane < K) {
+      x = __ldg(a.tokens + (long long)b * K + lane);
+      tok_ok = x >= 0 && x < a.V;
+      sm.tok[lane] = x;
     }
-    sm.bad = bad;
+    if (lane <= K && !greedy) sm.r[lane] = __ldg(a.uniforms + ob + lane);
+    const bool all_ok = __all_sync(0xffffffffu, tok_ok);
+    if (lane == 0)
+      sm.bad = !valid_temperature(T) ? (int)kDevBadTemperature : (all_ok ? 0 : (int)kDevBadToken);
+    if (all_ok && !greedy && valid_temperature(T) && lane < K) {
+      sm.xp[lane] = E::load_scalar(a.target, (ob + lane) * (long long)a.V + x);
+      sm.xq[lane] = E::load_scalar(a.draft, ((long long)b * K + lane) * (long long)a.V + x);
+    }
   }
+  if (!greedy)
+    for (int i = tid; i < 256; i += kP2Threads) sm.tab[i] = kExp2Table256[i];
   __syncthreads();
+  if (sm.bad && rank != 0) return;   // row-wide, so the same in every CTA of the cluster
 
-  const long long tb = (long long)b * (K + 1);   // first target row of b
-  const long long db = a.n_target_rows + (long long)b * K;  // first draft row of b (partials index)
+  // ---------------- wait for the streaming pass and the visibility of its writes
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // fold the tile partials into row statistics; one warp per row
+  // ---------------- fold tile partials into row statistics; one warp per row
+  const long long tb = ob;                               // first target row of b
+  const long long db = a.n_target_rows + (long long)b * K;  // first draft row of b
   const int nrows = greedy ? K + 1 : 2 * K + 1;
-  const float c32 = greedy ? 0.f : __fdiv_rn(kLog2eHi, T);
-  if (!sm.bad && (!greedy || rank == 0)) {
-    for (int r = warp; r < nrows; r += kP2Warps) {
-      const long long prow = (r <= K) ? tb + r : db + (r - K - 1);
+  if (!sm.bad) {
+    for (int rr = warp; rr < nrows; rr += kP2Warps) {
+      const long long prow = (rr <= K) ? tb + rr : db + (rr - K - 1);
       const float2* pp = a.partials + prow * a.tiles_per_row;
       if (greedy) {
         float best = SV_NEG_INF;
         int bi = 0x7fffffff;
-        for (int i = lane; i < a.tiles_per_row; i += 32) {
-          const float2 v = pp[i];
-          const int idx = __float_as_int(v.y);
-          if (v.x > best || (v.x == best && idx < bi)) {
-            best = v.x;
-            bi = idx;
+        for (int base = 0; base < a.tiles_per_row; base += 32 * 8) {
+          float2 v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int i = base + lane + 32 * j;
+            v[j] = i < a.tiles_per_row ? pp[i] : make_float2(SV_NEG_INF, __int_as_float(0x7fffffff));
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int idx = __float_as_int(v[j].y);
+            if (v[j].x > best || (v[j].x == best && idx < bi)) {
+              best = v[j].x;
+              bi = idx;
+            }
           }
         }
         const float m = warp_max(best);
         const int idx = warp_min_int(best == m ? bi : 0x7fffffff);
         if (lane == 0) {
-          sm.rowM[r] = m;
-          sm.rowArg[r] = idx;
+          sm.rowMC[rr] = m;
+          sm.rowArg[rr] = idx;
         }
       } else {
-        float m = SV_NEG_INF;
-        for (int i = lane; i < a.tiles_per_row; i += 32) m = fmaxf(m, pp[i].x);
-        m = warp_max(m);
-        float s = 0.f;
-        for (int i = lane; i < a.tiles_per_row; i += 32) {
-          const float2 v = pp[i];
-          if (v.x != SV_NEG_INF) s += v.y * ex2_approx(__fmul_rn(__fsub_rn(v.x, m), c32));
+        // loads first (independent), then the online fold
+        float mc = SV_NEG_INF, s = 0.f;
+        for (int base = 0; base < a.tiles_per_row; base += 32 * 8) {
+          float2 v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int i = base + lane + 32 * j;
+            v[j] = i < a.tiles_per_row ? pp[i] : make_float2(SV_NEG_INF, 0.f);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (v[j].x == SV_NEG_INF) continue;
+            if (v[j].x > mc) {
+              s = s * ex2_approx(__fsub_rn(mc, v[j].x)) + v[j].y;
+              mc = v[j].x;
+            } else {
+              s += v[j].y * ex2_approx(__fsub_rn(v[j].x, mc));
+            }
+          }
         }
-        s = warp_sum(s);
+        const float M = warp_max(mc);
+        float sv = (mc == SV_NEG_INF) ? 0.f : s * ex2_approx(__fsub_rn(mc, M));
+        sv = warp_sum(sv);
         if (lane == 0) {
-          sm.rowM[r] = m;
-          sm.rowS[r] = s;
+          sm.rowMC[rr] = M;
+          sm.rowS[rr] = sv;
         }
       }
     }
   }
   __syncthreads();
 
-  // ---------------------------------------------------------------- accept scan
-  const long long ob = (long long)b * (K + 1);
-  if (threadIdx.x == 0) {
+  // ---------------- acceptance scan: one lane per drafted position
+  const float c = greedy ? 0.f : log2e_over_f(T);
+  if (warp == 0) {
     int bad = sm.bad;
+    bool row_ok = true;
+    for (int rr = lane; !bad && rr < nrows; rr += 32) {
+      const float M = sm.rowMC[rr];
+      row_ok = row_ok && isfinite(M) && (greedy || (isfinite(sm.rowS[rr]) && sm.rowS[rr] > 0.f));
+    }
+    if (!bad && !__all_sync(0xffffffffu, row_ok)) bad = (int)kDevNonFinite;
     int n = K;
+    float lp = __int_as_float(0x7fffffff), lq = lp;
     if (!bad) {
-      for (int r = 0; r < nrows; ++r) {
-        const bool ok = isfinite(sm.rowM[r]) && (greedy || (isfinite(sm.rowS[r]) && sm.rowS[r] > 0.f));
-        if (!ok) bad = (int)kDevNonFinite;
+      bool reject = false;
+      if (greedy) {
+        reject = lane < K && sm.rowArg[lane] != sm.tok[lane];
+      } else if (lane < K) {
+        // log p_t(x_t) = (x c - MC) ln 2 - ln S, with x c - MC formed exactly by the FMA
+        constexpr float kLn2 = 0.693147180559945309f;
+        lp = __fmaf_rn(sm.xp[lane], c, -sm.rowMC[lane]) * kLn2 - logf(sm.rowS[lane]);
+        lq = __fmaf_rn(sm.xq[lane], c, -sm.rowMC[K + 1 + lane]) * kLn2 - logf(sm.rowS[K + 1 + lane]);
+        // r q < p  <=>  r < p / q = exp(log p - log q)
+        reject = !(sm.r[lane] < expf(lp - lq));
       }
+      const unsigned rej = __ballot_sync(0xffffffffu, reject);
+      n = rej ? __ffs(rej) - 1 : K;
     }
-    if (!bad && greedy && rank == 0) {
-      // "Caso ganancioso": accept while argmax(p_t) == x_t
-      for (int t = 0; t < K; ++t) {
-        if (sm.rowArg[t] != __ldg(a.tokens + (long long)b * K + t)) {
-          n = t;
-          break;
-        }
+    if (rank == 0) {
+      if (lane < K) {
+        if (a.logp_out) a.logp_out[(long long)b * K + lane] = bad || greedy ? __int_as_float(0x7fffffff) : lp;
+        if (a.logq_out) a.logq_out[(long long)b * K + lane] = bad || greedy ? __int_as_float(0x7fffffff) : lq;
       }
-    } else if (!bad && !greedy) {
-      const char* tgt = (const char*)a.target;
-      const char* drf = (const char*)a.draft;
-      n = -1;
-      for (int t = 0; t < K; ++t) {
-        const int x = __ldg(a.tokens + (long long)b * K + t);
-        const float xp = E::load_scalar(tgt, (tb + t) * (long long)a.V + x);
-        const float xq = E::load_scalar(drf, ((long long)b * K + t) * (long long)a.V + x);
-        // log p_t(x_t) = (z_x - m)/T - ln S
-        const float lp = __fdiv_rn(__fsub_rn(xp, sm.rowM[t]), T) - logf(sm.rowS[t]);
-        const float lq = __fdiv_rn(__fsub_rn(xq, sm.rowM[K + 1 + t]), T) - logf(sm.rowS[K + 1 + t]);
-        if (rank == 0) {
-          if (a.logp_out) a.logp_out[(long long)b * K + t] = lp;
-          if (a.logq_out) a.logq_out[(long long)b * K + t] = lq;
-        }
-        if (n < 0) {
-          const float r = __ldg(a.uniforms + ob + t);
-          // r q < p  <=>  r < p / q = exp(log p - log q)
-          if (!(r < expf(lp - lq))) n = t;
-        }
-      }
-      if (n < 0) n = K;
-    }
-    if (bad && rank == 0) {
-      atomicOr(a.err, (unsigned)bad);
-      a.accepted_len[b] = -1;
-      for (int t = 0; t <= K; ++t) a.out_tokens[ob + t] = -1;
-    }
-    if (rank == 0 && (bad || greedy)) {
-      for (int t = 0; t < K; ++t) {
-        if (a.logp_out) a.logp_out[(long long)b * K + t] = __int_as_float(0x7fffffff);
-        if (a.logq_out) a.logq_out[(long long)b * K + t] = __int_as_float(0x7fffffff);
-      }
-    }
-    if (!bad && rank == 0) {
-      a.accepted_len[b] = n;
-      for (int t = 0; t <= K; ++t) {
+      if (lane <= K) {
         int v = -1;
-        if (t < n) v = __ldg(a.tokens + (long long)b * K + t);
-        else if (t == n && greedy) v = sm.rowArg[n];
-        a.out_tokens[ob + t] = v;
+        if (!bad) {
+          if (lane < n) v = sm.tok[lane];
+          else if (lane == n && greedy) v = sm.rowArg[n];
+        }
+        if (!(lane == n && !greedy && !bad)) a.out_tokens[ob + lane] = v;
+      }
+      if (lane == 0) {
+        a.accepted_len[b] = bad ? -1 : n;
+        if (bad) atomicOr(a.err, (unsigned)bad);
       }
     }
-    sm.n = n;
-    sm.bad = bad;
+    if (lane == 0) {
+      sm.n = n;
+      sm.bad = bad;
+    }
   }
   __syncthreads();
-  if (sm.bad || greedy) return;   // uniform across the cluster; no shared memory was shared
+  if (sm.bad || greedy) return;   // the same in every CTA of the cluster
 
-  // ---------------------------------------------------------------- sampling
+  // ---------------- sampling at position n
   const int n = sm.n;
-  for (int i = threadIdx.x; i < 256; i += kP2Threads) sm.tab[i] = kExp2Table256[i];
   const long long rowbytes = (long long)a.V * E::kBytes;
-  const char* rowP = (const char*)a.target + (tb + n) * rowbytes;
-  const char* rowQ = (n < K) ? (const char*)a.draft + ((long long)b * K + n) * rowbytes : nullptr;
-  const float Mp = sm.rowM[n];
+  SampleCtx x;
+  x.rowP = (const char*)a.target + (tb + n) * rowbytes;
+  x.rowQ = (n < K) ? (const char*)a.draft + ((long long)b * K + n) * rowbytes : nullptr;
+  x.V = a.V;
+  x.g0 = rank * a.groups_per_cta;
+  x.ng = max(0, min(a.ngroups - x.g0, a.groups_per_cta));
+  x.MCp = sm.rowMC[n];
+  x.MCq = (n < K) ? sm.rowMC[K + 1 + n] : 0.f;
   const float Sp32 = sm.rowS[n];
-  const float Mq = (n < K) ? sm.rowM[K + 1 + n] : 0.f;
   const float Sq32 = (n < K) ? sm.rowS[K + 1 + n] : 1.f;
-  const float c_used = __fdiv_rn(Sp32, Sq32);
-  const float thp = kBigProb * Sp32;
-  const float thq = kBigProb * Sq32;
-  const DF L = log2e_over(T);
-  const float u = __ldg(a.uniforms + ob + K);
-  const int cv0 = rank * a.vecs_per_cta;
-  const int ncv = max(0, min(a.nvec - cv0, a.vecs_per_cta));
-  __syncthreads();
+  x.L = log2e_over(T);
+  // float32 path split of L with a strictly positive low part
+  x.c_hi = x.L.hi;
+  x.c_lo = x.L.lo;
+  if (!(x.c_lo > 0.f)) {
+    x.c_hi = __uint_as_float(__float_as_uint(x.L.hi) - 1u);   // one ulp below (L > 0)
+    x.c_lo = __fadd_rn(__fsub_rn(x.L.hi, x.c_hi), x.L.lo);
+  }
+  x.cw = __fdiv_rn(Sp32, Sq32);
+  x.thp = kBigProb * Sp32;
+  x.thq = kBigProb * Sq32;
+  const float u = sm.r[K];
 
   bool residual = n < K;
-  int token = -1;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    if (residual) {
-      sweep_slice<E, kAligned, true>(rowP, rowQ, a.V, cv0, ncv, Mp, Mq, L, c_used, thp, thq, sm, s_vec);
-    } else {
-      sweep_slice<E, kAligned, false>(rowP, rowQ, a.V, cv0, ncv, Mp, Mq, L, c_used, thp, thq, sm, s_vec);
-    }
+    DF Wt, Qt;
+    if (residual) sweep_slice<E, kAligned, true>(x, sm, s_part, Wt, Qt);
+    else sweep_slice<E, kAligned, false>(x, sm, s_part, Wt, Qt);
     cluster.sync();
-    if (threadIdx.x == 0) decide(cluster, cs, residual, c_used, u, a.vecs_per_cta, sm);
-    cluster.sync();   // every record has been read; the smem may be reused
+    if (tid < cs) sm.recs[tid] = *cluster.map_shared_rank(&sm.rec, tid);   // one remote read each
+    __syncthreads();
+    if (tid == 0) decide(sm.recs, cs, residual, x.cw, u, a.groups_per_cta, sm);
+    cluster.sync();   // every record has been read; shared memory may be reused
     if (sm.dec.need_p_fallback) {
-      residual = false;   // "residual" identically zero: draw from p_t instead
+      residual = false;   // the residual is zero everywhere: draw from p_t instead
+      x.rowQ = nullptr;
       continue;
     }
     if (rank == sm.dec.rstar) {
-      if (residual) {
-        token = locate<E, kAligned, true>(rowP, rowQ, a.V, cv0, ncv, Mp, Mq, L, c_used, thp, thq, sm, s_vec);
-      } else {
-        token = locate<E, kAligned, false>(rowP, rowQ, a.V, cv0, ncv, Mp, Mq, L, c_used, thp, thq, sm, s_vec);
-      }
-      if (threadIdx.x == 0) a.out_tokens[ob + n] = token;
+      const int token = residual ? locate<E, true>(x, sm, s_part, Wt, Qt)
+                                 : locate<E, false>(x, sm, s_part, Wt, Qt);
+      if (tid == 0) a.out_tokens[ob + n] = token;
     }
     break;
   }

@@ -35,6 +35,7 @@ from __future__ import annotations
 
 import dataclasses
 import os
+import sys
 from typing import Iterable, Sequence
 
 import numpy as np
@@ -213,6 +214,9 @@ def make(name: str, seed: int = 0, rows: Sequence[int] | None = None,
     temp = np.empty(nb, np.float32)
     if workers is None:
         workers = 1
+    main_file = getattr(sys.modules.get("__main__"), "__file__", None)
+    if workers > 1 and not (main_file and os.path.exists(main_file)):
+        workers = 1   # spawn children must re-import __main__; stdin/REPL has nothing to import
     chunks = [rows[i::workers] for i in range(workers)] if workers > 1 else [rows]
     if workers > 1 and nb > 1:
         import multiprocessing as mp
@@ -247,8 +251,8 @@ def custom(target: np.ndarray, draft: np.ndarray, draft_tokens: Iterable[Iterabl
            uniforms: np.ndarray, temperature: np.ndarray, dtype: str = "f32",
            name: str = "custom") -> Workload:
     """Wrap hand-built float64 logits as a workload (rounded to ``dtype``)."""
-    target = np.asarray(target, np.float64)
-    draft = np.asarray(draft, np.float64)
+    target = np.ascontiguousarray(target, np.float64)
+    draft = np.ascontiguousarray(draft, np.float64)
     B, K1, V = target.shape
     return Workload(name, B, K1 - 1, V, dtype, _store(target, dtype), _store(draft, dtype),
                     np.asarray(draft_tokens, np.int32).reshape(B, K1 - 1),

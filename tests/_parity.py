@@ -41,6 +41,17 @@ class ParityReport:
                             self.failures + o.failures)
 
 
+def _logprob_err(gpu, ref):
+    """Largest |difference|; equal infinities (a -inf logit) count as exact."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    same = (gpu == ref)
+    with np.errstate(invalid="ignore"):
+        d = np.where(same, 0.0, np.abs(gpu - ref))
+    d = np.where(np.isnan(d), np.inf, d)
+    return float(d.max()) if d.size else 0.0
+
+
 def check_structure(accepted, out_tokens, draft_tokens, V):
     """Properties that hold for every row at any size."""
     B, K1 = out_tokens.shape
@@ -84,7 +95,7 @@ def compare(ref, accepted, out_tokens, logp, logq, temperature, rows=None) -> Pa
             continue
         rep.stochastic_rows += 1
         if logp is not None:
-            err = max(np.abs(logp[g] - ref.logp[i]).max(), np.abs(logq[g] - ref.logq[i]).max())
+            err = max(_logprob_err(logp[g], ref.logp[i]), _logprob_err(logq[g], ref.logq[i]))
             if not err <= LOGPROB_ATOL:
                 rep.failures.append((g, f"log-prob error {err}"))
             rep.max_logprob_err = max(rep.max_logprob_err, float(err))

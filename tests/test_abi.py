@@ -45,11 +45,11 @@ def test_every_declared_symbol_is_exported(N):
 
 
 def test_workspace_bytes_arithmetic(N):
-    # 256-byte header + 8 bytes per 4 KB tile of every target and draft row
+    # 256-byte header + 8 bytes per 2 KB tile of every target and draft row
     B, K, V = 64, 4, 128256
-    tiles = -(-V // 2048)
+    tiles = -(-V // 1024)
     assert N.spec_verify_workspace_bytes(B, K, V, N.SV_BF16) == 256 + (B * (K + 1) + B * K) * tiles * 8
-    tiles32 = -(-V // 1024)
+    tiles32 = -(-V // 512)
     assert N.spec_verify_workspace_bytes(B, K, V, N.SV_F32) == 256 + (B * (K + 1) + B * K) * tiles32 * 8
     assert N.spec_verify_workspace_bytes(0, 4, 1000, N.SV_F32) == 256
     for bad in ((-1, 4, 10, 0), (1, 0, 10, 0), (1, 17, 10, 0), (1, 4, 0, 0), (1, 4, 10, 2),
