@@ -55,6 +55,22 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(seed: int, rank: int) -> int:
+    """Every rank verifies its own batch: weak scaling, no shared data."""
+    return seed + rank
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time (gloo all-reduce on a CPU tensor)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -220,7 +236,7 @@ def run_ours(args):
     b.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = synth.make(args.workload, seed=args.seed + rank, workers=synth.default_workers())
+    w = synth.make(args.workload, seed=rank_seed(args.seed, rank), workers=synth.default_workers())
     dt_torch = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     dtype_code = N.SV_BF16 if w.dtype == "bf16" else N.SV_F32
     B, K, V = w.B, w.K, w.V
@@ -254,12 +270,6 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
     # ---- warm-up, then the timed region (device events on the launching stream)
     for i in range(args.warmup):
@@ -275,7 +285,7 @@ def run_ours(args):
         call(copies[i % len(copies)])
     ev1.record(stream)
     barrier()
-    t_ms = max_over_ranks(ev0.elapsed_time(ev1))
+    t_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     gpu_launches = 2 * args.steps
     accepted = acc.cpu().numpy()
     if args.profile:
@@ -345,7 +355,7 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = d2h_acc.numel() * 4 + d2h_tok.numel() * 4
 
