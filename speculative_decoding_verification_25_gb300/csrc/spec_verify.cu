@@ -109,6 +109,29 @@ void cluster_geometry(int V, int dtype, int* cs, int* ngroups, int* gpc) {
 
 bool aligned_to(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace: [header][counters][tile partials][slice records][group weights].
+// The two launches use the header (row flags) and the tile partials; every
+// word they read was written earlier in the same call, so no part of the
+// workspace needs initialising.
+struct Layout {
+  size_t ctr, ctr_bytes, partials, recs, gparts, total;
+};
+Layout layout(int B, int K, int V, int dtype) {
+  Layout L;
+  const long long rows = (long long)B * (K + 1) + (long long)B * K;
+  int cs, ngroups, gpc;
+  cluster_geometry(V, dtype, &cs, &ngroups, &gpc);
+  L.ctr = kHeaderBytes;
+  L.ctr_bytes = (size_t)(3 + 2 * (long long)B) * sizeof(int);
+  L.partials = align_up(L.ctr + L.ctr_bytes, 256);
+  L.recs = align_up(L.partials + (size_t)(rows * tiles_per_row(V, dtype)) * sizeof(float2), 256);
+  L.gparts = align_up(L.recs + (size_t)B * cs * sizeof(sv::CtaRecord), 256);
+  L.total = L.gparts + (size_t)B * ngroups * sizeof(float4);
+  return L;
+}
+
 }  // namespace
 
 namespace {
@@ -160,7 +183,7 @@ int launch_row_stats(const void* target_logits, const void* draft_logits, int dt
   ra.tiles_per_row = (int)tpr;
   ra.n_tiles = (n_target_rows + (long long)B * K) * tpr;
   ra.n_target_rows = (int)n_target_rows;
-  ra.partials = (float2*)((char*)workspace + kHeaderBytes);
+  ra.partials = (float2*)((char*)workspace + layout(B, K, V, dtype).partials);
   ra.err = (unsigned*)workspace;
   // persistent grid: every SM filled once; every warp a contiguous tile range
   const int threads = sv::kP1Threads;
@@ -197,7 +220,7 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
   aa.n_target_rows = B * (K + 1);
   aa.ngroups = ngroups;
   aa.groups_per_cta = gpc;
-  aa.partials = (const float2*)((const char*)workspace + kHeaderBytes);
+  aa.partials = (const float2*)((const char*)workspace + layout(B, K, V, dtype).partials);
   aa.err = (unsigned*)workspace;
   aa.accepted_len = accepted_len;
   aa.out_tokens = out_tokens;
@@ -250,8 +273,7 @@ int spec_verify_max_vocab(int dtype) {
 
 size_t spec_verify_workspace_bytes(int B, int K, int V, int dtype) {
   if (!shape_ok(B, K, V, dtype)) return 0;
-  const long long rows = (long long)B * (K + 1) + (long long)B * K;
-  return kHeaderBytes + (size_t)(rows * tiles_per_row(V, dtype)) * sizeof(float2);
+  return layout(B, K, V, dtype).total;
 }
 
 const char* spec_verify_status_string(int status) {

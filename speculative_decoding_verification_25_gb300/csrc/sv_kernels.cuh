@@ -480,6 +480,21 @@ __device__ __noinline__ void large_terms(const SampleCtx& x, AcceptSmem& sm, int
   sums[3] = accQ;
 }
 
+// Per-thread sums over a contiguous run of `ng` group weights: the prefix
+// structure the locate step scans.  Thread t owns groups [t*cpt, (t+1)*cpt).
+__device__ __forceinline__ void chunk_sums(const float4* part, int ng, DF& Wt, DF& Qt) {
+  const int cpt = (ng + kP2Threads - 1) / kP2Threads;
+  const int a0 = min(ng, (int)threadIdx.x * cpt), a1 = min(ng, a0 + cpt);
+  DF W{0.f, 0.f}, Q{0.f, 0.f};
+  for (int gl = a0; gl < a1; ++gl) {
+    const float4 p4 = part[gl];
+    W = df_add(W, DF{p4.x, p4.y});
+    Q = df_add(Q, DF{p4.z, p4.w});
+  }
+  Wt = W;
+  Qt = Q;
+}
+
 // One sweep of this CTA over its groups of the sampled row(s).  Per-group
 // weights go to part[] (w.hi, w.lo, q.hi, q.lo); the CTA record to sm.rec.
 // The per-thread sums of part[] over the thread's contiguous run of groups
@@ -553,18 +568,8 @@ __device__ void sweep_slice(const SampleCtx& x, AcceptSmem& sm, float4* part, DF
   }
   __syncthreads();   // part[] complete
 
-  // per-thread sums over a contiguous run of groups: the prefix structure
-  const int cpt = (x.ng + kP2Threads - 1) / kP2Threads;
-  const int a0 = min(x.ng, tid * cpt), a1 = min(x.ng, a0 + cpt);
-  DF W{0.f, 0.f}, Q{0.f, 0.f};
-  for (int gl = a0; gl < a1; ++gl) {
-    const float4 p4 = part[gl];
-    W = df_add(W, DF{p4.x, p4.y});
-    Q = df_add(Q, DF{p4.z, p4.w});
-  }
-  Wt = W;
-  Qt = Q;
-  DF tot[4] = {W, Q, accP, accQ};
+  chunk_sums(part, x.ng, Wt, Qt);
+  DF tot[4] = {Wt, Qt, accP, accQ};
   block_sum4(tot, sm);
   const int last = block_max_int(lastg, sm);
   if (tid == 0) {
@@ -747,23 +752,16 @@ __device__ int locate(const SampleCtx& x, AcceptSmem& sm, const float4* part, DF
   return token;
 }
 
-template <typename E, bool kAligned>
-__global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptArgs a) {
-  extern __shared__ __align__(16) float4 s_part[];
-  __shared__ AcceptSmem sm;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int cs = (int)cluster.num_blocks();
-  const int rank = (int)cluster.block_rank();
-  const int b = blockIdx.x / cs;
-  const int K = a.K;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const long long ob = (long long)b * (K + 1);
-
-  // ---------------- prologue: inputs only, overlaps the streaming pass
-  const float T = __ldg(a.temperature + b);
+// ---------------------------------------------------------------- accept stages
+// Inputs of batch row b (warp 0): tokens, uniforms, the 2K gathered logits
+// at the drafted tokens, and the row's validity (sm.bad).  Reads inputs
+// only, so it may run before the statistics exist.
+template <typename E>
+__device__ void accept_inputs(const AcceptArgs& a, int b, float T, AcceptSmem& sm) {
+  const int K = a.K, lane = threadIdx.x & 31;
   const bool greedy = (T == 0.f);
-  if (rank != 0 && (greedy || !valid_temperature(T))) return;   // rank 0 alone handles these
-  if (warp == 0) {
+  const long long ob = (long long)b * (K + 1);
+  if ((threadIdx.x >> 5) == 0) {
     int x = 0;
     bool tok_ok = true;
     if (lane < K) {
@@ -781,141 +779,147 @@ __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptA
     }
   }
   if (!greedy)
-    for (int i = tid; i < 256; i += kP2Threads) sm.tab[i] = kExp2Table256[i];
-  __syncthreads();
-  if (sm.bad && rank != 0) return;   // row-wide, so the same in every CTA of the cluster
+    for (int i = threadIdx.x; i < 256; i += kP2Threads) sm.tab[i] = kExp2Table256[i];
+}
 
-  // ---------------- wait for the streaming pass and the visibility of its writes
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  // ---------------- fold tile partials into row statistics; one warp per row
-  const long long tb = ob;                               // first target row of b
-  const long long db = a.n_target_rows + (long long)b * K;  // first draft row of b
+// Fold the tile partials of batch row b into row statistics, one warp per
+// row: (MC, S) for tempered rows, (max, lowest argmax) for greedy rows.
+__device__ void fold_row_stats(const AcceptArgs& a, int b, bool greedy, AcceptSmem& sm) {
+  const int K = a.K, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long tb = (long long)b * (K + 1);
+  const long long db = a.n_target_rows + (long long)b * K;
   const int nrows = greedy ? K + 1 : 2 * K + 1;
-  if (!sm.bad) {
-    for (int rr = warp; rr < nrows; rr += kP2Warps) {
-      const long long prow = (rr <= K) ? tb + rr : db + (rr - K - 1);
-      const float2* pp = a.partials + prow * a.tiles_per_row;
-      if (greedy) {
-        float best = SV_NEG_INF;
-        int bi = 0x7fffffff;
-        for (int base = 0; base < a.tiles_per_row; base += 32 * 8) {
-          float2 v[8];
+  for (int rr = warp; rr < nrows; rr += kP2Warps) {
+    const long long prow = (rr <= K) ? tb + rr : db + (rr - K - 1);
+    const float2* pp = a.partials + prow * a.tiles_per_row;
+    if (greedy) {
+      float best = SV_NEG_INF;
+      int bi = 0x7fffffff;
+      for (int base = 0; base < a.tiles_per_row; base += 32 * 8) {
+        float2 v[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int i = base + lane + 32 * j;
-            v[j] = i < a.tiles_per_row ? pp[i] : make_float2(SV_NEG_INF, __int_as_float(0x7fffffff));
-          }
+        for (int j = 0; j < 8; ++j) {
+          const int i = base + lane + 32 * j;
+          v[j] = i < a.tiles_per_row ? pp[i] : make_float2(SV_NEG_INF, __int_as_float(0x7fffffff));
+        }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int idx = __float_as_int(v[j].y);
-            if (v[j].x > best || (v[j].x == best && idx < bi)) {
-              best = v[j].x;
-              bi = idx;
-            }
+        for (int j = 0; j < 8; ++j) {
+          const int idx = __float_as_int(v[j].y);
+          if (v[j].x > best || (v[j].x == best && idx < bi)) {
+            best = v[j].x;
+            bi = idx;
           }
         }
-        const float m = warp_max(best);
-        const int idx = warp_min_int(best == m ? bi : 0x7fffffff);
-        if (lane == 0) {
-          sm.rowMC[rr] = m;
-          sm.rowArg[rr] = idx;
-        }
-      } else {
-        // loads first (independent), then the online fold
-        float mc = SV_NEG_INF, s = 0.f;
-        for (int base = 0; base < a.tiles_per_row; base += 32 * 8) {
-          float2 v[8];
+      }
+      const float m = warp_max(best);
+      const int idx = warp_min_int(best == m ? bi : 0x7fffffff);
+      if (lane == 0) {
+        sm.rowMC[rr] = m;
+        sm.rowArg[rr] = idx;
+      }
+    } else {
+      // loads first (independent), then the online fold
+      float mc = SV_NEG_INF, s = 0.f;
+      for (int base = 0; base < a.tiles_per_row; base += 32 * 8) {
+        float2 v[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int i = base + lane + 32 * j;
-            v[j] = i < a.tiles_per_row ? pp[i] : make_float2(SV_NEG_INF, 0.f);
-          }
+        for (int j = 0; j < 8; ++j) {
+          const int i = base + lane + 32 * j;
+          v[j] = i < a.tiles_per_row ? pp[i] : make_float2(SV_NEG_INF, 0.f);
+        }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (v[j].x == SV_NEG_INF) continue;
-            if (v[j].x > mc) {
-              s = s * ex2_approx(__fsub_rn(mc, v[j].x)) + v[j].y;
-              mc = v[j].x;
-            } else {
-              s += v[j].y * ex2_approx(__fsub_rn(v[j].x, mc));
-            }
+        for (int j = 0; j < 8; ++j) {
+          if (v[j].x == SV_NEG_INF) continue;
+          if (v[j].x > mc) {
+            s = s * ex2_approx(__fsub_rn(mc, v[j].x)) + v[j].y;
+            mc = v[j].x;
+          } else {
+            s += v[j].y * ex2_approx(__fsub_rn(v[j].x, mc));
           }
         }
-        const float M = warp_max(mc);
-        float sv = (mc == SV_NEG_INF) ? 0.f : s * ex2_approx(__fsub_rn(mc, M));
-        sv = warp_sum(sv);
-        if (lane == 0) {
-          sm.rowMC[rr] = M;
-          sm.rowS[rr] = sv;
-        }
+      }
+      const float M = warp_max(mc);
+      float sv = (mc == SV_NEG_INF) ? 0.f : s * ex2_approx(__fsub_rn(mc, M));
+      sv = warp_sum(sv);
+      if (lane == 0) {
+        sm.rowMC[rr] = M;
+        sm.rowS[rr] = sv;
       }
     }
   }
-  __syncthreads();
+}
 
-  // ---------------- acceptance scan: one lane per drafted position
+// Acceptance scan (warp 0): one lane per drafted position; sets sm.n and
+// sm.bad.  With `write`, also writes accepted_len, the log-probabilities and
+// every out_tokens slot except the one a tempered row still has to sample.
+__device__ void accept_scan(const AcceptArgs& a, int b, float T, bool write, AcceptSmem& sm) {
+  const int K = a.K, lane = threadIdx.x & 31;
+  if ((threadIdx.x >> 5) != 0) return;
+  const bool greedy = (T == 0.f);
+  const long long ob = (long long)b * (K + 1);
+  const int nrows = greedy ? K + 1 : 2 * K + 1;
   const float c = greedy ? 0.f : log2e_over_f(T);
-  if (warp == 0) {
-    int bad = sm.bad;
-    bool row_ok = true;
-    for (int rr = lane; !bad && rr < nrows; rr += 32) {
-      const float M = sm.rowMC[rr];
-      row_ok = row_ok && isfinite(M) && (greedy || (isfinite(sm.rowS[rr]) && sm.rowS[rr] > 0.f));
+  int bad = sm.bad;
+  bool row_ok = true;
+  for (int rr = lane; !bad && rr < nrows; rr += 32) {
+    const float M = sm.rowMC[rr];
+    row_ok = row_ok && isfinite(M) && (greedy || (isfinite(sm.rowS[rr]) && sm.rowS[rr] > 0.f));
+  }
+  if (!bad && !__all_sync(0xffffffffu, row_ok)) bad = (int)kDevNonFinite;
+  int n = K;
+  float lp = __int_as_float(0x7fffffff), lq = lp;
+  if (!bad) {
+    bool reject = false;
+    if (greedy) {
+      reject = lane < K && sm.rowArg[lane] != sm.tok[lane];
+    } else if (lane < K) {
+      // log p_t(x_t) = (x c - MC) ln 2 - ln S, with x c - MC formed exactly by the FMA
+      constexpr float kLn2 = 0.693147180559945309f;
+      lp = __fmaf_rn(sm.xp[lane], c, -sm.rowMC[lane]) * kLn2 - logf(sm.rowS[lane]);
+      lq = __fmaf_rn(sm.xq[lane], c, -sm.rowMC[K + 1 + lane]) * kLn2 - logf(sm.rowS[K + 1 + lane]);
+      // r q < p  <=>  r < p / q = exp(log p - log q)
+      reject = !(sm.r[lane] < expf(lp - lq));
     }
-    if (!bad && !__all_sync(0xffffffffu, row_ok)) bad = (int)kDevNonFinite;
-    int n = K;
-    float lp = __int_as_float(0x7fffffff), lq = lp;
-    if (!bad) {
-      bool reject = false;
-      if (greedy) {
-        reject = lane < K && sm.rowArg[lane] != sm.tok[lane];
-      } else if (lane < K) {
-        // log p_t(x_t) = (x c - MC) ln 2 - ln S, with x c - MC formed exactly by the FMA
-        constexpr float kLn2 = 0.693147180559945309f;
-        lp = __fmaf_rn(sm.xp[lane], c, -sm.rowMC[lane]) * kLn2 - logf(sm.rowS[lane]);
-        lq = __fmaf_rn(sm.xq[lane], c, -sm.rowMC[K + 1 + lane]) * kLn2 - logf(sm.rowS[K + 1 + lane]);
-        // r q < p  <=>  r < p / q = exp(log p - log q)
-        reject = !(sm.r[lane] < expf(lp - lq));
-      }
-      const unsigned rej = __ballot_sync(0xffffffffu, reject);
-      n = rej ? __ffs(rej) - 1 : K;
+    const unsigned rej = __ballot_sync(0xffffffffu, reject);
+    n = rej ? __ffs(rej) - 1 : K;
+  }
+  if (write) {
+    if (lane < K) {
+      if (a.logp_out) a.logp_out[(long long)b * K + lane] = bad || greedy ? __int_as_float(0x7fffffff) : lp;
+      if (a.logq_out) a.logq_out[(long long)b * K + lane] = bad || greedy ? __int_as_float(0x7fffffff) : lq;
     }
-    if (rank == 0) {
-      if (lane < K) {
-        if (a.logp_out) a.logp_out[(long long)b * K + lane] = bad || greedy ? __int_as_float(0x7fffffff) : lp;
-        if (a.logq_out) a.logq_out[(long long)b * K + lane] = bad || greedy ? __int_as_float(0x7fffffff) : lq;
+    if (lane <= K) {
+      int v = -1;
+      if (!bad) {
+        if (lane < n) v = sm.tok[lane];
+        else if (lane == n && greedy) v = sm.rowArg[n];
       }
-      if (lane <= K) {
-        int v = -1;
-        if (!bad) {
-          if (lane < n) v = sm.tok[lane];
-          else if (lane == n && greedy) v = sm.rowArg[n];
-        }
-        if (!(lane == n && !greedy && !bad)) a.out_tokens[ob + lane] = v;
-      }
-      if (lane == 0) {
-        a.accepted_len[b] = bad ? -1 : n;
-        if (bad) atomicOr(a.err, (unsigned)bad);
-      }
+      if (!(lane == n && !greedy && !bad)) a.out_tokens[ob + lane] = v;
     }
     if (lane == 0) {
-      sm.n = n;
-      sm.bad = bad;
+      a.accepted_len[b] = bad ? -1 : n;
+      if (bad) atomicOr(a.err, (unsigned)bad);
     }
   }
-  __syncthreads();
-  if (sm.bad || greedy) return;   // the same in every CTA of the cluster
+  if (lane == 0) {
+    sm.n = n;
+    sm.bad = bad;
+  }
+}
 
-  // ---------------- sampling at position n
-  const int n = sm.n;
+// What the sampling sweep needs about position n of batch row b, for the
+// groups [g0, g0 + ng) of the sampled row(s).
+template <typename E>
+__device__ SampleCtx sample_ctx(const AcceptArgs& a, int b, float T, int g0, int ng,
+                                const AcceptSmem& sm) {
+  const int K = a.K, n = sm.n;
   const long long rowbytes = (long long)a.V * E::kBytes;
   SampleCtx x;
-  x.rowP = (const char*)a.target + (tb + n) * rowbytes;
+  x.rowP = (const char*)a.target + ((long long)b * (K + 1) + n) * rowbytes;
   x.rowQ = (n < K) ? (const char*)a.draft + ((long long)b * K + n) * rowbytes : nullptr;
   x.V = a.V;
-  x.g0 = rank * a.groups_per_cta;
-  x.ng = max(0, min(a.ngroups - x.g0, a.groups_per_cta));
+  x.g0 = g0;
+  x.ng = ng;
   x.MCp = sm.rowMC[n];
   x.MCq = (n < K) ? sm.rowMC[K + 1 + n] : 0.f;
   const float Sp32 = sm.rowS[n];
@@ -931,9 +935,41 @@ __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptA
   x.cw = __fdiv_rn(Sp32, Sq32);
   x.thp = kBigProb * Sp32;
   x.thq = kBigProb * Sq32;
-  const float u = sm.r[K];
+  return x;
+}
 
-  bool residual = n < K;
+// ---------------------------------------------------------------- the cluster kernel
+template <typename E, bool kAligned>
+__global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptArgs a) {
+  extern __shared__ __align__(16) float4 s_part[];
+  __shared__ AcceptSmem sm;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cs = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int b = blockIdx.x / cs;
+  const int tid = threadIdx.x;
+
+  // prologue: inputs only, overlaps the streaming pass
+  const float T = __ldg(a.temperature + b);
+  const bool greedy = (T == 0.f);
+  if (rank != 0 && (greedy || !valid_temperature(T))) return;   // rank 0 alone handles these
+  accept_inputs<E>(a, b, T, sm);
+  __syncthreads();
+  if (sm.bad && rank != 0) return;   // row-wide, so the same in every CTA of the cluster
+
+  // wait for the streaming pass and the visibility of its writes
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!sm.bad) fold_row_stats(a, b, greedy, sm);
+  __syncthreads();
+  accept_scan(a, b, T, rank == 0, sm);
+  __syncthreads();
+  if (sm.bad || greedy) return;   // the same in every CTA of the cluster
+
+  // sampling at position n
+  const int g0 = rank * a.groups_per_cta;
+  SampleCtx x = sample_ctx<E>(a, b, T, g0, max(0, min(a.ngroups - g0, a.groups_per_cta)), sm);
+  const float u = sm.r[a.K];
+  bool residual = sm.n < a.K;
   for (int attempt = 0; attempt < 2; ++attempt) {
     DF Wt, Qt;
     if (residual) sweep_slice<E, kAligned, true>(x, sm, s_part, Wt, Qt);
@@ -951,7 +987,7 @@ __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptA
     if (rank == sm.dec.rstar) {
       const int token = residual ? locate<E, true>(x, sm, s_part, Wt, Qt)
                                  : locate<E, false>(x, sm, s_part, Wt, Qt);
-      if (tid == 0) a.out_tokens[ob + n] = token;
+      if (tid == 0) a.out_tokens[(long long)b * (a.K + 1) + sm.n] = token;
     }
     break;
   }

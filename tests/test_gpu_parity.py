@@ -9,7 +9,7 @@ import pytest
 from speculative_decoding_verification_25_gb300 import synth
 
 from _parity import check_structure, compare
-from gpu_util import device_tensors, run_gpu, run_oracle
+from gpu_util import device_tensors, run_gpu, run_gpu_stages, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -105,6 +105,37 @@ def test_large_vocab_stress_full_size():
     print("large_vocab_stress parity:", rep)
     assert rep.greedy_rows == 256
     _assert_parity(rep, 0)
+
+
+# ---------------------------------------------------------------- the two-launch entry points
+
+@pytest.mark.parametrize("name,seed", [("tiny_stochastic", 3), ("tiny_greedy", 3),
+                                       ("greedy_batch", 0), ("llama3_stochastic", 1)])
+def test_two_launch_stages_match_oracle(name, seed):
+    w = synth.make(name, seed=seed, workers=synth.default_workers())
+    g = run_gpu_stages(w)
+    ref = run_oracle(w)
+    assert not check_structure(g["accepted"], g["out_tokens"], w.draft_tokens, w.V)
+    rep = compare(ref, g["accepted"], g["out_tokens"], g["logp"], g["logq"], w.temperature)
+    _assert_parity(rep, 0)
+
+
+def test_shapes_change_on_one_workspace():
+    """Calls of different shapes share one (never initialised) workspace."""
+    import torch
+    from speculative_decoding_verification_25_gb300 import api
+    ws = torch.full((64 << 20,), 0xAB, dtype=torch.uint8, device="cuda:0")   # garbage
+    for name, rows in (("greedy_batch", range(7)), ("llama3_stochastic", range(12)),
+                       ("tiny_stochastic", None), ("llama3_stochastic", range(3))):
+        w = synth.make(name, seed=2, rows=rows)
+        d = device_tensors(w)
+        r = api.spec_verify(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
+                            d["temperature"], want_logprobs=True, workspace=ws)
+        torch.cuda.synchronize()
+        ref = run_oracle(w, workers=1)
+        rep = compare(ref, r.accepted_len.cpu().numpy(), r.out_tokens.cpu().numpy(),
+                      r.logp.cpu().numpy(), r.logq.cpu().numpy(), w.temperature)
+        _assert_parity(rep, 0)
 
 
 # ---------------------------------------------------------------- small shapes and edges
