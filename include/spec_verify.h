@@ -117,7 +117,7 @@ int spec_verify(const void* target_logits, const void* draft_logits, int dtype,
  * same stream, inputs and workspace give exactly spec_verify's result.
  *
  * spec_verify_row_stats streams every target row and the draft rows of
- * rows with T > 0 once and leaves one partial per 4 KB tile in the
+ * rows with T > 0 once and leaves one partial per 2 KB tile in the
  * workspace: (tile max m, sum of e^((x - m)/T)) for the softmax
  * normaliser, or (max logit, its lowest index) for T == 0 rows.  It also
  * clears the device flag word.

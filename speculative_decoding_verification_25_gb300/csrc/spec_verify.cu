@@ -3,7 +3,7 @@
 //
 // One call = two launches on the caller's stream:
 //   1. sv_row_stats_kernel, a persistent grid (SM count x resident CTAs)
-//      whose warps stream contiguous ranges of 4 KB row tiles;
+//      whose warps stream contiguous ranges of 2 KB row tiles;
 //   2. sv_accept_sample_kernel, one thread-block cluster per batch row,
 //      launched with programmatic dependent launch so its CTAs are resident
 //      and waiting when the streaming pass retires.
