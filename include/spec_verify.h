@@ -60,6 +60,7 @@ extern "C" {
 #define SV_ERR_ALIGN 4      /* a pointer is not aligned to its element (workspace: 16 bytes) */
 #define SV_ERR_WORKSPACE 5  /* workspace_bytes < spec_verify_workspace_bytes(B, K, V, dtype) */
 #define SV_ERR_CUDA 6       /* a CUDA runtime call failed (launch, attribute, copy) */
+#define SV_ERR_TOO_LARGE 7  /* spec_verify_static: the shape needs more than SV_STATIC_SCRATCH_BYTES */
 
 /* device-side row flags, OR-ed into the workspace error word */
 #define SV_DEV_BAD_TEMPERATURE 1u  /* T negative, NaN, infinite, or in (0, FLT_MIN) */
@@ -147,6 +148,49 @@ int spec_verify_accept_sample(const void* target_logits, const void* draft_logit
  * SV_ERR_NULL or SV_ERR_CUDA.
  */
 int spec_verify_device_errors(const void* workspace, void* stream, uint32_t* flags);
+
+/*
+ * Bytes of the library's own device scratch used by spec_verify_static
+ * (8 MiB, one array per device, part of the loaded module).
+ */
+#define SV_STATIC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * spec_verify without a caller workspace and without any allocation.
+ *
+ * The lesson that states the rule has no counterpart of this call: it is a
+ * convenience of this library for callers that cannot hand over, or must
+ * not allocate, device scratch at call time.  Arguments, outputs and
+ * return codes are those of spec_verify minus `workspace` and
+ * `workspace_bytes`; the kernels and their arithmetic are the same, so the
+ * results equal spec_verify's.
+ *
+ * The scratch is a file-scope device array of SV_STATIC_SCRATCH_BYTES bytes
+ * (256-byte aligned) in this library.  Shapes whose
+ * spec_verify_workspace_bytes(B, K, V, dtype) exceeds that size are
+ * rejected with SV_ERR_TOO_LARGE before anything touches the device (at
+ * V = 128256 bf16 and K = 4 that admits B up to 114).  Nothing in
+ * the scratch must start at zero: the streaming launch resets its error
+ * word and every partial is written before it is read.
+ *
+ * Setup: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and keeps it; a failed lookup returns
+ * SV_ERR_CUDA.  Make that first call on each device before any stream
+ * capture begins.  No call allocates memory (no cudaMalloc, no cudaFree,
+ * no allocating library routine).
+ *
+ * There is ONE scratch per device: calls that may overlap on the device
+ * (different streams without an ordering between them, or several host
+ * threads) race on it and may return wrong tokens.  Order all calls on a
+ * device, e.g. on one stream.  The device row flags of these calls are
+ * kept in that scratch and are not readable through this interface; error
+ * rows still show as accepted_len = -1.
+ */
+int spec_verify_static(const void* target_logits, const void* draft_logits, int dtype,
+                       const int32_t* draft_tokens, const float* uniforms,
+                       const float* temperature, int B, int K, int V,
+                       int32_t* accepted_len, int32_t* out_tokens,
+                       float* logp_out, float* logq_out, void* stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* spec_verify_status_string(int status);

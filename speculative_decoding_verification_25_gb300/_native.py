@@ -21,12 +21,14 @@ SV_ERR_DTYPE = 3
 SV_ERR_ALIGN = 4
 SV_ERR_WORKSPACE = 5
 SV_ERR_CUDA = 6
+SV_ERR_TOO_LARGE = 7
 
 SV_DEV_BAD_TEMPERATURE = 1
 SV_DEV_BAD_TOKEN = 2
 SV_DEV_NONFINITE = 4
 
 SV_MAX_K = 16
+SV_STATIC_SCRATCH_BYTES = 8 << 20
 
 # every function of include/spec_verify.h: (restype, argtypes)
 _P = ctypes.c_void_p
@@ -40,6 +42,7 @@ _SIG = {
     "spec_verify_accept_sample": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P,
                                        ctypes.c_size_t, _P]),
     "spec_verify_device_errors": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
+    "spec_verify_static": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "spec_verify_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -107,6 +110,15 @@ def spec_verify_accept_sample_raw(target_ptr, draft_ptr, dtype, tokens_ptr, unif
                                                 uniforms_ptr, temperature_ptr, B, K, V,
                                                 accepted_ptr, out_tokens_ptr, logp_ptr, logq_ptr,
                                                 workspace_ptr, workspace_bytes, stream_handle))
+
+
+def spec_verify_static_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr,
+                           temperature_ptr, B, K, V, accepted_ptr, out_tokens_ptr, logp_ptr,
+                           logq_ptr, stream_handle) -> int:
+    """spec_verify on the library's static scratch (no workspace argument)."""
+    return int(load().spec_verify_static(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr,
+                                         temperature_ptr, B, K, V, accepted_ptr, out_tokens_ptr,
+                                         logp_ptr, logq_ptr, stream_handle))
 
 
 def spec_verify_device_errors(workspace_ptr, stream_handle) -> int:

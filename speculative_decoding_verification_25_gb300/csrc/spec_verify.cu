@@ -27,9 +27,17 @@ struct DeviceCache {
   int sm_count = 0;
   int row_stats_blocks_per_sm[2][2] = {{0, 0}, {0, 0}};  // [dtype][aligned]
   cudaError_t init_error = cudaSuccess;
+  // device address of g_static_scratch, looked up by the first
+  // spec_verify_static call on this device
+  std::once_flag static_once;
+  void* static_scratch = nullptr;
+  cudaError_t static_error = cudaSuccess;
 };
 
 DeviceCache g_devices[kMaxDevices];
+
+// Scratch of spec_verify_static: one array per device, loaded with the module.
+__device__ __align__(256) unsigned char g_static_scratch[SV_STATIC_SCRATCH_BYTES];
 
 int vec_of(int dtype) { return dtype == SV_BF16 ? 8 : 4; }
 int elt_of(int dtype) { return dtype == SV_BF16 ? 2 : 4; }
@@ -261,6 +269,17 @@ DeviceCache* current_device_cache() {
   return dc;
 }
 
+// Device address of this device's g_static_scratch (nullptr if the lookup
+// failed); the lookup runs once per device.
+void* static_scratch(DeviceCache* dc) {
+  std::call_once(dc->static_once, [dc]() {
+    void* p = nullptr;
+    dc->static_error = cudaGetSymbolAddress(&p, g_static_scratch);
+    dc->static_scratch = (dc->static_error == cudaSuccess) ? p : nullptr;
+  });
+  return dc->static_scratch;
+}
+
 }  // namespace
 
 extern "C" {
@@ -285,6 +304,8 @@ const char* spec_verify_status_string(int status) {
     case SV_ERR_ALIGN: return "a pointer is not aligned to its element size (workspace: 16 bytes)";
     case SV_ERR_WORKSPACE: return "workspace smaller than spec_verify_workspace_bytes()";
     case SV_ERR_CUDA: return "a CUDA runtime call failed";
+    case SV_ERR_TOO_LARGE:
+      return "shape needs more scratch than spec_verify_static holds (SV_STATIC_SCRATCH_BYTES)";
     default: return "unknown status";
   }
 }
@@ -335,6 +356,32 @@ int spec_verify(const void* target_logits, const void* draft_logits, int dtype,
   return launch_accept_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
                               temperature, B, K, V, accepted_len, out_tokens, logp_out, logq_out,
                               workspace, s);
+}
+
+int spec_verify_static(const void* target_logits, const void* draft_logits, int dtype,
+                       const int32_t* draft_tokens, const float* uniforms,
+                       const float* temperature, int B, int K, int V, int32_t* accepted_len,
+                       int32_t* out_tokens, float* logp_out, float* logq_out, void* stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (!shape_ok(B, K, V, dtype)) return SV_ERR_SHAPE;
+  if (B == 0) return SV_OK;
+  if (spec_verify_workspace_bytes(B, K, V, dtype) > (size_t)SV_STATIC_SCRATCH_BYTES)
+    return SV_ERR_TOO_LARGE;
+  DeviceCache* dc = current_device_cache();
+  if (!dc) return SV_ERR_CUDA;
+  void* scratch = static_scratch(dc);
+  if (!scratch) return SV_ERR_CUDA;
+  const int st = validate(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                          B, K, V, accepted_len, out_tokens, logp_out, logq_out, scratch,
+                          (size_t)SV_STATIC_SCRATCH_BYTES, true);
+  if (st != SV_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int r = launch_row_stats(target_logits, draft_logits, dtype, temperature, B, K, V,
+                                 scratch, dc, s);
+  if (r != SV_OK) return r;
+  return launch_accept_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
+                              temperature, B, K, V, accepted_len, out_tokens, logp_out, logq_out,
+                              scratch, s);
 }
 
 int spec_verify_device_errors(const void* workspace, void* stream, uint32_t* flags) {

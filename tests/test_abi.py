@@ -71,8 +71,8 @@ def test_max_vocab_covers_the_workloads(N):
 
 
 def test_status_strings(N):
-    for s in range(7):
-        assert N.status_string(s)
+    for s in range(8):
+        assert N.status_string(s) != "unknown status"
     assert N.status_string(99) == "unknown status"
 
 
@@ -111,6 +111,24 @@ def test_validation_errors_launch_nothing(N):
 def test_empty_batch_is_a_no_op(N):
     assert _call(N, B=0, target=None, draft=None, tokens=None, uniforms=None, temperature=None,
                  accepted=None, out=None, ws=None, ws_bytes=0) == N.SV_OK
+
+
+def test_static_entry_point_rejects_before_touching_the_device(N):
+    """spec_verify_static: argument and size checks come before any CUDA call."""
+    def call(dtype=N.SV_BF16, B=2, K=4, V=1024):
+        return N.spec_verify_static_raw(FAKE, FAKE, dtype, FAKE, FAKE, FAKE, B, K, V, FAKE, FAKE,
+                                        None, None, None)
+    assert call(dtype=5) == N.SV_ERR_DTYPE
+    assert call(K=0) == N.SV_ERR_SHAPE
+    assert call(B=-3) == N.SV_ERR_SHAPE
+    assert call(B=0) == N.SV_OK
+    # the largest batch at the Llama-3 vocabulary that fits the static scratch, and one more
+    fits = [B for B in range(1, 400)
+            if N.spec_verify_workspace_bytes(B, 4, 128256, N.SV_BF16) <= N.SV_STATIC_SCRATCH_BYTES]
+    assert fits and fits == list(range(1, fits[-1] + 1)) and fits[-1] >= 64
+    assert call(B=fits[-1] + 1, V=128256) == N.SV_ERR_TOO_LARGE
+    assert call(B=256, K=8, V=152064, dtype=N.SV_F32) == N.SV_ERR_TOO_LARGE
+    assert "static" in N.status_string(N.SV_ERR_TOO_LARGE)
 
 
 def test_device_errors_rejects_null(N):
