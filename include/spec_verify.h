@@ -104,6 +104,9 @@ int spec_verify_max_vocab(int dtype);
  * B == 0 is a no-op (pointers may then be NULL).  Returns SV_OK or an
  * SV_ERR_* code; on an error code nothing has been launched.  Two calls
  * that share a workspace must be ordered on the device (same stream).
+ *
+ * Enqueues the two launches of spec_verify_row_stats and
+ * spec_verify_accept_sample below.
  */
 int spec_verify(const void* target_logits, const void* draft_logits, int dtype,
                 const int32_t* draft_tokens, const float* uniforms,
@@ -169,9 +172,9 @@ int spec_verify_device_errors(const void* workspace, void* stream, uint32_t* fla
  * (256-byte aligned) in this library.  Shapes whose
  * spec_verify_workspace_bytes(B, K, V, dtype) exceeds that size are
  * rejected with SV_ERR_TOO_LARGE before anything touches the device (at
- * V = 128256 bf16 and K = 4 that admits B up to 114).  Nothing in
- * the scratch must start at zero: the streaming launch resets its error
- * word and every partial is written before it is read.
+ * V = 128256 bf16 and K = 4 that admits B up to 924).  Nothing in the
+ * scratch must start at zero: the streaming launch resets its flag word and
+ * writes every partial before the accept launch reads it.
  *
  * Setup: the first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) and keeps it; a failed lookup returns

@@ -1,7 +1,8 @@
 // Host side of spec_verify: argument checks, launch geometry and the C ABI
 // declared in include/spec_verify.h.
 //
-// One call = two launches on the caller's stream:
+// One call (spec_verify, spec_verify_static, or spec_verify_row_stats +
+// spec_verify_accept_sample) = two launches on the caller's stream:
 //   1. sv_row_stats_kernel, a persistent grid (SM count x resident CTAs)
 //      whose warps stream contiguous ranges of 2 KB row tiles;
 //   2. sv_accept_sample_kernel, one thread-block cluster per batch row,
@@ -119,25 +120,14 @@ bool aligned_to(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: [header][counters][tile partials][slice records][group weights].
-// The two launches use the header (row flags) and the tile partials; every
-// word they read was written earlier in the same call, so no part of the
-// workspace needs initialising.
-struct Layout {
-  size_t ctr, ctr_bytes, partials, recs, gparts, total;
-};
-Layout layout(int B, int K, int V, int dtype) {
-  Layout L;
+// Workspace: a 256-byte header (the row-flag word at offset 0), then one
+// float2 partial per tile of every target and draft row.  The streaming
+// launch clears the flag word and writes every partial the accept launch
+// reads, so no part of the workspace needs initialising.
+size_t partials_offset() { return align_up(kHeaderBytes, 256); }
+size_t workspace_total(int B, int K, int V, int dtype) {
   const long long rows = (long long)B * (K + 1) + (long long)B * K;
-  int cs, ngroups, gpc;
-  cluster_geometry(V, dtype, &cs, &ngroups, &gpc);
-  L.ctr = kHeaderBytes;
-  L.ctr_bytes = (size_t)(3 + 2 * (long long)B) * sizeof(int);
-  L.partials = align_up(L.ctr + L.ctr_bytes, 256);
-  L.recs = align_up(L.partials + (size_t)(rows * tiles_per_row(V, dtype)) * sizeof(float2), 256);
-  L.gparts = align_up(L.recs + (size_t)B * cs * sizeof(sv::CtaRecord), 256);
-  L.total = L.gparts + (size_t)B * ngroups * sizeof(float4);
-  return L;
+  return partials_offset() + (size_t)(rows * tiles_per_row(V, dtype)) * sizeof(float2);
 }
 
 }  // namespace
@@ -191,7 +181,7 @@ int launch_row_stats(const void* target_logits, const void* draft_logits, int dt
   ra.tiles_per_row = (int)tpr;
   ra.n_tiles = (n_target_rows + (long long)B * K) * tpr;
   ra.n_target_rows = (int)n_target_rows;
-  ra.partials = (float2*)((char*)workspace + layout(B, K, V, dtype).partials);
+  ra.partials = (float2*)((char*)workspace + partials_offset());
   ra.err = (unsigned*)workspace;
   // persistent grid: every SM filled once; every warp a contiguous tile range
   const int threads = sv::kP1Threads;
@@ -228,7 +218,7 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
   aa.n_target_rows = B * (K + 1);
   aa.ngroups = ngroups;
   aa.groups_per_cta = gpc;
-  aa.partials = (const float2*)((const char*)workspace + layout(B, K, V, dtype).partials);
+  aa.partials = (const float2*)((const char*)workspace + partials_offset());
   aa.err = (unsigned*)workspace;
   aa.accepted_len = accepted_len;
   aa.out_tokens = out_tokens;
@@ -292,7 +282,7 @@ int spec_verify_max_vocab(int dtype) {
 
 size_t spec_verify_workspace_bytes(int B, int K, int V, int dtype) {
   if (!shape_ok(B, K, V, dtype)) return 0;
-  return layout(B, K, V, dtype).total;
+  return workspace_total(B, K, V, dtype);
 }
 
 const char* spec_verify_status_string(int status) {

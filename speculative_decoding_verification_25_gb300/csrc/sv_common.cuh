@@ -87,50 +87,26 @@ __device__ __forceinline__ void load_vec(const void* row, long long v, int V, ui
   }
 }
 
-// ----------------------------------------------------------------- bulk async copies
-// One-dimensional cp.async.bulk from global to this CTA's shared memory,
-// completed through an mbarrier transaction count (no tensor map needed).
+// ----------------------------------------------------------------- async copies
+// 16-byte global -> shared copies (cp.async, L2 only) that a thread later
+// reads back itself: cp.async.wait_group makes a thread's own completed
+// copies visible to it, so no barrier is needed between the lanes.
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-// make barrier initialisation visible to the async proxy
-__device__ __forceinline__ void mbar_init_fence() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-               "r"(bytes)
+__device__ __forceinline__ void lds16(uint32_t addr, uint32_t (&w)[4]) {
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "r"(addr)
                : "memory");
-}
-// generic-proxy accesses to shared memory before async-proxy writes to it
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst_smem)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-// Bounded wait on an mbarrier phase.  Returns false if the phase did not
-// complete within the limit (the caller flags the row; nothing spins forever).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase) {
-  const uint32_t a = smem_addr(bar);
-  for (int it = 0; it < (1 << 22); ++it) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(a), "r"(phase)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
 }
 
 // ----------------------------------------------------------------- packed float32 pairs

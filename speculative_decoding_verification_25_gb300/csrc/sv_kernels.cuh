@@ -6,7 +6,9 @@
 //   writes one partial per tile:
 //     tempered rows:  (MC, S) with S = sum of 2^(x*c - MC), c = log2(e)/T
 //                     rounded to float32 and MC a float32 shift >= max x*c;
-//     greedy rows:    (max logit, lowest index holding it).
+//     greedy rows:    (max logit, ~(lowest index holding it)), the index
+//                     stored complemented (no written partial is all-zero
+//                     bits).
 //   A lane folds its tiles into running values and the warp reduces them
 //   only where its range leaves a row; the other tiles of that stretch get
 //   the neutral partial (-inf, 0).  Draft rows of greedy rows are not read.
@@ -41,7 +43,8 @@ constexpr int kP2Warps = kP2Threads / 32;
 constexpr int kGroupVecs = 4;                     // a sampling group: 64 B of each row
 constexpr int kMaxGroupsPerThread = 8;
 constexpr int kMaxClusterSize = 16;
-constexpr int kQueueCap = 32;                     // large-term queue entries per warp
+constexpr int kBigCap = 1024;                     // large terms listed per sweep (more: evaluated inline)
+constexpr uint32_t kBigNone = 0xffffffffu;        // a claimed list slot that stays unused
 // A term whose probability exceeds this is evaluated in double-float
 // during sampling; smaller terms use the float32 path.
 constexpr float kBigProb = 1.0e-4f;
@@ -171,14 +174,14 @@ __device__ __forceinline__ void flush_stretch(float2* pp, int first, int last, b
   if (greedy) {
     const float m = warp_max(st.best);
     const int idx = warp_min_int(st.best == m ? st.bi : 0x7fffffff);
-    part = make_float2(m, __int_as_float(idx));
+    part = make_float2(m, __int_as_float(~idx));
   } else {
     const float M = warp_max(st.mc);
     float sv = (st.mc == SV_NEG_INF) ? 0.f : st.s * ex2_approx(__fsub_rn(st.mc, M));
     sv = warp_sum(sv);
     part = make_float2(M, sv);
   }
-  const float2 neutral = make_float2(SV_NEG_INF, greedy ? __int_as_float(0x7fffffff) : 0.f);
+  const float2 neutral = make_float2(SV_NEG_INF, greedy ? __int_as_float(~0x7fffffff) : 0.f);
   for (int k = first + lane; k <= last; k += 32) pp[k] = (k == last) ? part : neutral;
 }
 
@@ -187,6 +190,7 @@ struct RowParams {
   bool active, greedy;
   float c;
   const char* rowp;
+  RowParams() = default;
   __device__ __forceinline__ RowParams(const RowStatsArgs& a, int row, int elem_bytes) {
     int b, r;
     bool is_draft;
@@ -246,6 +250,17 @@ __global__ void __launch_bounds__(kP1Threads, 4) sv_row_stats_kernel(RowStatsArg
     }
     tile += ti1 - ti0;
   }
+}
+
+// ============================================================== sampling group
+// The accept/sample code runs on a group of kP2Threads threads that starts
+// at a warp boundary and ends the CTA (the whole CTA in
+// sv_accept_sample_kernel).  gtid() is the thread's index in the group;
+// gsync() is a barrier over the group only (named barrier 1), so a kernel
+// may give its other warps other work.
+__device__ __forceinline__ int gtid() { return (int)threadIdx.x - (int)blockDim.x + kP2Threads; }
+__device__ __forceinline__ void gsync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kP2Threads) : "memory");
 }
 
 // ============================================================== accept + sample
@@ -309,11 +324,13 @@ struct AcceptSmem {
   int group_pick;
   DF tau_group;
   DF warp_tot[kP2Warps];
-  // large terms: per-lane raw words of the current group (staged only by
-  // lanes that have one), the warp's queue of terms and their results
-  uint4 raw[kP2Warps][32][2 * kGroupVecs];
-  float2 qx[kP2Warps][kQueueCap];
-  float4 qres[kP2Warps][kQueueCap];
+  // large terms of the current sweep: their positions ((local group << 5) |
+  // element), their double-float results (w, q), and for every (step,
+  // thread) the slice of the list its group owns ((offset << 8) | count)
+  int nbig;
+  uint32_t bigpos[kBigCap];
+  float4 bigres[kBigCap];
+  uint32_t bigref[kMaxGroupsPerThread][kP2Threads];
   DF red1[4];
 };
 
@@ -372,32 +389,32 @@ __device__ __forceinline__ void eval_pair(float xp, float xq, const SampleCtx& s
 
 // Block-wide sum of four double-floats; every thread gets the totals.
 __device__ __forceinline__ void block_sum4(DF (&v)[4], AcceptSmem& sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = gtid() & 31, warp = gtid() >> 5;
 #pragma unroll
   for (int i = 0; i < 4; ++i) v[i] = warp_sum_df(v[i]);
   if (lane == 0)
 #pragma unroll
     for (int i = 0; i < 4; ++i) sm.red[warp][i] = v[i];
-  __syncthreads();
-  if (threadIdx.x < 4) {
+  gsync();
+  if (gtid() < 4) {
     DF t{0.f, 0.f};
-    for (int w = 0; w < kP2Warps; ++w) t = df_add(t, sm.red[w][threadIdx.x]);
-    sm.red1[threadIdx.x] = t;
+    for (int w = 0; w < kP2Warps; ++w) t = df_add(t, sm.red[w][gtid()]);
+    sm.red1[gtid()] = t;
   }
-  __syncthreads();
+  gsync();
 #pragma unroll
   for (int i = 0; i < 4; ++i) v[i] = sm.red1[i];
 }
 
 __device__ __forceinline__ int block_max_int(int v, AcceptSmem& sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = gtid() & 31, warp = gtid() >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
   if (lane == 0) sm.redi[warp] = v;
-  __syncthreads();
+  gsync();
   int t = sm.redi[0];
   for (int w = 1; w < kP2Warps; ++w) t = max(t, sm.redi[w]);
-  __syncthreads();
+  gsync();
   return t;
 }
 
@@ -408,86 +425,40 @@ __device__ __forceinline__ void load_group(const char* row, int g, int V, uint32
   for (int j = 0; j < kGroupVecs; ++j) load_vec<E, kAligned>(row, (long long)g * kGroupVecs + j, V, w[j]);
 }
 
-// The large terms of one group step, in double-float.  Every lane with a
-// set bit in `big` has staged its group's raw words in sm.raw[warp][lane];
-// the warp lays all terms out in one queue (lane order), evaluates up to
-// kQueueCap at a time, one per lane, and each lane folds back its own
-// contiguous slice of results into (wg, qg) and the totals (accP, accQ).
+// Double-float weight of one large term at row position idx: w (and the
+// q that goes with a positive w), plus e^p and e^q for the row totals.
 template <typename E, bool kResidual>
-__device__ __noinline__ void large_terms(const SampleCtx& x, AcceptSmem& sm, int warp, int lane,
-                                         unsigned big, DF* sums) {
-  const int cnt = __popc(big);
-  int off = cnt;   // inclusive scan of the counts
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, off, o);
-    if (lane >= o) off += v;
+__device__ __forceinline__ void big_term(const SampleCtx& x, const float2* tab, long long idx, DF& w,
+                                         DF& q, DF& ep, DF& eq) {
+  ep = big_exp(E::load_scalar(x.rowP, idx), x.MCp, x, tab);
+  w = ep;
+  q = DF{0.f, 0.f};
+  eq = DF{0.f, 0.f};
+  if (kResidual) {
+    eq = big_exp(E::load_scalar(x.rowQ, idx), x.MCq, x, tab);
+    const DF d = df_sub(ep, df_mul_f(eq, x.cw));
+    w = df_pos(d) ? d : DF{0.f, 0.f};
+    q = df_pos(d) ? eq : DF{0.f, 0.f};
   }
-  const int total = __shfl_sync(0xffffffffu, off, 31);
-  off -= cnt;
-  DF wg = sums[0], qg = sums[1], accP = sums[2], accQ = sums[3];
-  const uint32_t* rawp = reinterpret_cast<const uint32_t*>(sm.raw[warp][lane]);
-  for (int base = 0; base < total; base += kQueueCap) {
-    // lay out this window of the queue
-    {
-      unsigned m = big;
-      int idx = off;
-      while (m) {
-        const int e = __ffs(m) - 1;
-        m &= m - 1u;
-        if (idx >= base && idx < base + kQueueCap) {
-          const int j = e / E::kVec, k = e % E::kVec;
-          const uint32_t wpk[4] = {rawp[4 * j], rawp[4 * j + 1], rawp[4 * j + 2], rawp[4 * j + 3]};
-          float xq = 0.f;
-          if (kResidual) {
-            const int jq = kGroupVecs + j;
-            const uint32_t wqk[4] = {rawp[4 * jq], rawp[4 * jq + 1], rawp[4 * jq + 2], rawp[4 * jq + 3]};
-            xq = E::elem(wqk, k);
-          }
-          sm.qx[warp][idx - base] = make_float2(E::elem(wpk, k), xq);
-        }
-        ++idx;
-      }
-    }
-    __syncwarp();
-    const int n = min(kQueueCap, total - base);
-    for (int i = lane; i < n; i += 32) {
-      const float2 xx = sm.qx[warp][i];
-      const DF epd = big_exp(xx.x, x.MCp, x, sm.tab);
-      DF w = epd, q{0.f, 0.f}, Q{0.f, 0.f};
-      if (kResidual) {
-        Q = big_exp(xx.y, x.MCq, x, sm.tab);
-        const DF d = df_sub(epd, df_mul_f(Q, x.cw));
-        w = df_pos(d) ? d : DF{0.f, 0.f};
-        q = df_pos(d) ? Q : DF{0.f, 0.f};
-      }
-      sm.qres[warp][i] = make_float4(w.hi, w.lo, q.hi, q.lo);
-      // the totals do not care which lane adds them
-      accP = df_add(accP, epd);
-      if (kResidual) accQ = df_add(accQ, Q);
-    }
-    __syncwarp();
-    for (int i = max(off, base); i < min(off + cnt, base + n); ++i) {
-      const float4 r = sm.qres[warp][i - base];
-      wg = df_add(wg, DF{r.x, r.y});
-      qg = df_add(qg, DF{r.z, r.w});
-    }
-    __syncwarp();
-  }
-  sums[0] = wg;
-  sums[1] = qg;
-  sums[2] = accP;
-  sums[3] = accQ;
+}
+
+// A group weight; kCg: global memory written by other CTAs of this launch,
+// read from L2.
+template <bool kCg>
+__device__ __forceinline__ float4 load_part(const float4* p) {
+  if constexpr (kCg) return __ldcg(p);
+  else return *p;
 }
 
 // Per-thread sums over a contiguous run of `ng` group weights: the prefix
 // structure the locate step scans.  Thread t owns groups [t*cpt, (t+1)*cpt).
+template <bool kCg = false>
 __device__ __forceinline__ void chunk_sums(const float4* part, int ng, DF& Wt, DF& Qt) {
   const int cpt = (ng + kP2Threads - 1) / kP2Threads;
-  const int a0 = min(ng, (int)threadIdx.x * cpt), a1 = min(ng, a0 + cpt);
+  const int a0 = min(ng, (int)gtid() * cpt), a1 = min(ng, a0 + cpt);
   DF W{0.f, 0.f}, Q{0.f, 0.f};
   for (int gl = a0; gl < a1; ++gl) {
-    const float4 p4 = part[gl];
+    const float4 p4 = load_part<kCg>(part + gl);
     W = df_add(W, DF{p4.x, p4.y});
     Q = df_add(Q, DF{p4.z, p4.w});
   }
@@ -495,16 +466,26 @@ __device__ __forceinline__ void chunk_sums(const float4* part, int ng, DF& Wt, D
   Qt = Q;
 }
 
-// One sweep of this CTA over its groups of the sampled row(s).  Per-group
-// weights go to part[] (w.hi, w.lo, q.hi, q.lo); the CTA record to sm.rec.
-// The per-thread sums of part[] over the thread's contiguous run of groups
-// come back in Wt, Qt (the locate step scans them).
+// One sweep of this group of threads over its groups of the sampled row(s).
+// Per-group weights go to part[] (w.hi, w.lo, q.hi, q.lo); the record to
+// sm.rec.  The per-thread sums of part[] over the thread's contiguous run of
+// groups come back in Wt, Qt (the locate step scans them).
+//
+// Small terms are summed in float32 as they stream by.  A large term only
+// leaves its position in a list shared by the group; once the float32 pass
+// is done, all threads evaluate the list in double-float (one term each),
+// and every thread adds the results of its own groups' terms back into
+// their weights.  A thread whose terms find the list full evaluates them
+// itself.
 template <typename E, bool kAligned, bool kResidual>
 __device__ void sweep_slice(const SampleCtx& x, AcceptSmem& sm, float4* part, DF& Wt, DF& Qt) {
-  const int tid = threadIdx.x;
+  constexpr int kGroupElems = kGroupVecs * E::kVec;
+  const int tid = gtid();
+  const int lane = tid & 31;
   DF accP{0.f, 0.f}, accQ{0.f, 0.f};
   int lastg = -1;
-  const int lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) sm.nbig = 0;
+  gsync();
   const int iters = (x.ng + kP2Threads - 1) / kP2Threads;   // the same for every thread
   for (int it = 0; it < iters; ++it) {
     const int gl = it * kP2Threads + tid;
@@ -544,29 +525,90 @@ __device__ void sweep_slice(const SampleCtx& x, AcceptSmem& sm, float4* part, DF
         }
       }
     }
-    DF sums[4] = {DF{0.f, 0.f}, DF{0.f, 0.f}, accP, accQ};
+    if (!kResidual) sp = sw;
+    DF wg{sw, 0.f}, qg{sq, 0.f};
+    // claim list slots for this step's large terms (one atomic per warp)
+    uint32_t ref = 0;
     if (__any_sync(0xffffffffu, big != 0u)) {
-      if (big) {
+      const int cnt = __popc(big);
+      int inc = cnt;
 #pragma unroll
-        for (int j = 0; j < kGroupVecs; ++j) {
-          sm.raw[warp][lane][j] = make_uint4(wp[j][0], wp[j][1], wp[j][2], wp[j][3]);
-          if (kResidual) sm.raw[warp][lane][kGroupVecs + j] = make_uint4(wq[j][0], wq[j][1], wq[j][2], wq[j][3]);
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
+      }
+      int base = 0;
+      if (lane == 31) base = atomicAdd(&sm.nbig, inc);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      const int total = __shfl_sync(0xffffffffu, inc, 31);
+      const int off = base + inc - cnt;
+      if (base + total <= kBigCap) {
+        unsigned m = big;
+        int o = off;
+        while (m) {
+          const int e = __ffs(m) - 1;
+          m &= m - 1u;
+          sm.bigpos[o++] = ((uint32_t)gl << 5) | (uint32_t)e;
+        }
+        ref = ((uint32_t)off << 8) | (uint32_t)cnt;
+      } else {
+        // the list is full: mark this warp's claimed slots unused and
+        // evaluate the terms here
+        for (int o = off; o < off + cnt && o < kBigCap; ++o) sm.bigpos[o] = kBigNone;
+        unsigned m = big;
+        while (m) {
+          const int e = __ffs(m) - 1;
+          m &= m - 1u;
+          DF w, q, ep, eq;
+          big_term<E, kResidual>(x, sm.tab, (long long)g * kGroupElems + e, w, q, ep, eq);
+          wg = df_add(wg, w);
+          qg = df_add(qg, q);
+          accP = df_add(accP, ep);
+          accQ = df_add(accQ, eq);
         }
       }
-      __syncwarp();
-      large_terms<E, kResidual>(x, sm, warp, lane, big, sums);
     }
-    if (!kResidual) sp = sw;
-    const DF wg = df_add_f(sums[0], sw);
-    const DF qg = df_add_f(sums[1], sq);
+    sm.bigref[it][tid] = ref;
     if (valid) {
       part[gl] = make_float4(wg.hi, wg.lo, qg.hi, qg.lo);
       if (df_pos(wg)) lastg = g;
     }
-    accP = df_add_f(sums[2], sp);
-    accQ = df_add_f(sums[3], sQ);
+    accP = df_add_f(accP, sp);
+    accQ = df_add_f(accQ, sQ);
   }
-  __syncthreads();   // part[] complete
+  gsync();   // the list is complete
+
+  // every listed large term, one per thread
+  const int nb = min(sm.nbig, kBigCap);
+  for (int e = tid; e < nb; e += kP2Threads) {
+    const uint32_t pos = sm.bigpos[e];
+    if (pos == kBigNone) continue;
+    DF w, q, ep, eq;
+    big_term<E, kResidual>(x, sm.tab, ((long long)x.g0 + (pos >> 5)) * kGroupElems + (pos & 31u), w,
+                           q, ep, eq);
+    sm.bigres[e] = make_float4(w.hi, w.lo, q.hi, q.lo);
+    accP = df_add(accP, ep);   // the totals do not care which thread adds them
+    accQ = df_add(accQ, eq);
+  }
+  gsync();
+
+  // fold the results back into the groups that own them
+  for (int it = 0; it < iters; ++it) {
+    const uint32_t ref = sm.bigref[it][tid];
+    const int cnt = (int)(ref & 0xffu);
+    if (cnt == 0) continue;
+    const int gl = it * kP2Threads + tid;
+    float4 p4 = part[gl];
+    DF wg{p4.x, p4.y}, qg{p4.z, p4.w};
+    for (int o = (int)(ref >> 8); o < (int)(ref >> 8) + cnt; ++o) {
+      const float4 r = sm.bigres[o];
+      wg = df_add(wg, DF{r.x, r.y});
+      qg = df_add(qg, DF{r.z, r.w});
+    }
+    part[gl] = make_float4(wg.hi, wg.lo, qg.hi, qg.lo);
+    if (df_pos(wg)) lastg = max(lastg, x.g0 + gl);
+  }
+  gsync();   // part[] complete
 
   chunk_sums(part, x.ng, Wt, Qt);
   DF tot[4] = {Wt, Qt, accP, accQ};
@@ -630,9 +672,9 @@ __device__ void decide(const CtaRecord* recs, int cs, bool residual, float cw, f
 }
 
 // Find the token inside CTA rstar (all threads of that CTA).
-template <typename E, bool kResidual>
+template <typename E, bool kResidual, bool kCg = false>
 __device__ int locate(const SampleCtx& x, AcceptSmem& sm, const float4* part, DF Wt, DF Qt) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = gtid(), lane = tid & 31, warp = tid >> 5;
   const DF dc = sm.dec.dc;
   const DF huge{3.0e38f, 0.f};
   const int cpt = (x.ng + kP2Threads - 1) / kP2Threads;
@@ -655,7 +697,7 @@ __device__ int locate(const SampleCtx& x, AcceptSmem& sm, const float4* part, DF
       if (lane >= o) inc = df_add(inc, up);
     }
     if (lane == 31) sm.warp_tot[warp] = inc;
-    __syncthreads();
+    gsync();
     DF wpre{0.f, 0.f};
     for (int w = 0; w < warp; ++w) wpre = df_add(wpre, sm.warp_tot[w]);
     DF exc = df_shfl_up(inc, 1);
@@ -667,7 +709,7 @@ __device__ int locate(const SampleCtx& x, AcceptSmem& sm, const float4* part, DF
       if (df_lt(tau, inc)) atomicMin(&sm.pick_thread, tid);
       atomicMax(&sm.pick_last, tid);
     }
-    __syncthreads();
+    gsync();
     int ts = sm.pick_thread;
     bool at_top = false;
     if (ts == 0x7fffffff) {   // rounding pushed tau past this CTA's mass
@@ -680,7 +722,7 @@ __device__ int locate(const SampleCtx& x, AcceptSmem& sm, const float4* part, DF
       DF tg = huge;
       const int a0 = min(x.ng, tid * cpt), a1 = min(x.ng, a0 + cpt);
       for (int gl = a0; gl < a1; ++gl) {
-        const float4 p4 = part[gl];
+        const float4 p4 = load_part<kCg>(part + gl);
         DF wc{p4.x, p4.y};
         if (kResidual) wc = df_sub(wc, df_mul(dc, DF{p4.z, p4.w}));
         const DF nxt = df_add(run, wc);
@@ -700,7 +742,7 @@ __device__ int locate(const SampleCtx& x, AcceptSmem& sm, const float4* part, DF
       sm.group_pick = gs;
       sm.tau_group = tg;
     }
-    __syncthreads();
+    gsync();
     gstar = sm.group_pick;
     tau_g = sm.tau_group;
     if (tau_g.hi >= huge.hi) last_mode = true;
@@ -758,10 +800,10 @@ __device__ int locate(const SampleCtx& x, AcceptSmem& sm, const float4* part, DF
 // only, so it may run before the statistics exist.
 template <typename E>
 __device__ void accept_inputs(const AcceptArgs& a, int b, float T, AcceptSmem& sm) {
-  const int K = a.K, lane = threadIdx.x & 31;
+  const int K = a.K, lane = gtid() & 31;
   const bool greedy = (T == 0.f);
   const long long ob = (long long)b * (K + 1);
-  if ((threadIdx.x >> 5) == 0) {
+  if ((gtid() >> 5) == 0) {
     int x = 0;
     bool tok_ok = true;
     if (lane < K) {
@@ -779,72 +821,77 @@ __device__ void accept_inputs(const AcceptArgs& a, int b, float T, AcceptSmem& s
     }
   }
   if (!greedy)
-    for (int i = threadIdx.x; i < 256; i += kP2Threads) sm.tab[i] = kExp2Table256[i];
+    for (int i = gtid(); i < 256; i += kP2Threads) sm.tab[i] = kExp2Table256[i];
+}
+
+// One warp folds the tpr tile partials of one row: (MC, S) for a tempered
+// row, (max logit, lowest index holding it as int bits) for a greedy row
+// (whose partials hold the complemented index).  Every lane returns the
+// result.
+__device__ __forceinline__ float2 fold_partials(const float2* pp, int tpr, bool greedy, int lane) {
+  if (greedy) {
+    float best = SV_NEG_INF;
+    int bi = 0x7fffffff;
+    for (int base = 0; base < tpr; base += 32 * 8) {
+      float2 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + lane + 32 * j;
+        v[j] = i < tpr ? __ldcg(pp + i) : make_float2(SV_NEG_INF, __int_as_float(~0x7fffffff));
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int idx = ~__float_as_int(v[j].y);
+        if (v[j].x > best || (v[j].x == best && idx < bi)) {
+          best = v[j].x;
+          bi = idx;
+        }
+      }
+    }
+    const float m = warp_max(best);
+    const int idx = warp_min_int(best == m ? bi : 0x7fffffff);
+    return make_float2(m, __int_as_float(idx));
+  }
+  // loads first (independent), then the online fold
+  float mc = SV_NEG_INF, s = 0.f;
+  for (int base = 0; base < tpr; base += 32 * 8) {
+    float2 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = base + lane + 32 * j;
+      v[j] = i < tpr ? __ldcg(pp + i) : make_float2(SV_NEG_INF, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (v[j].x == SV_NEG_INF) continue;
+      if (v[j].x > mc) {
+        s = s * ex2_approx(__fsub_rn(mc, v[j].x)) + v[j].y;
+        mc = v[j].x;
+      } else {
+        s += v[j].y * ex2_approx(__fsub_rn(v[j].x, mc));
+      }
+    }
+  }
+  const float M = warp_max(mc);
+  float sv = (mc == SV_NEG_INF) ? 0.f : s * ex2_approx(__fsub_rn(mc, M));
+  sv = warp_sum(sv);
+  return make_float2(M, sv);
 }
 
 // Fold the tile partials of batch row b into row statistics, one warp per
 // row: (MC, S) for tempered rows, (max, lowest argmax) for greedy rows.
 __device__ void fold_row_stats(const AcceptArgs& a, int b, bool greedy, AcceptSmem& sm) {
-  const int K = a.K, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int K = a.K, lane = gtid() & 31, warp = gtid() >> 5;
   const long long tb = (long long)b * (K + 1);
   const long long db = a.n_target_rows + (long long)b * K;
   const int nrows = greedy ? K + 1 : 2 * K + 1;
   for (int rr = warp; rr < nrows; rr += kP2Warps) {
     const long long prow = (rr <= K) ? tb + rr : db + (rr - K - 1);
-    const float2* pp = a.partials + prow * a.tiles_per_row;
-    if (greedy) {
-      float best = SV_NEG_INF;
-      int bi = 0x7fffffff;
-      for (int base = 0; base < a.tiles_per_row; base += 32 * 8) {
-        float2 v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = base + lane + 32 * j;
-          v[j] = i < a.tiles_per_row ? pp[i] : make_float2(SV_NEG_INF, __int_as_float(0x7fffffff));
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int idx = __float_as_int(v[j].y);
-          if (v[j].x > best || (v[j].x == best && idx < bi)) {
-            best = v[j].x;
-            bi = idx;
-          }
-        }
-      }
-      const float m = warp_max(best);
-      const int idx = warp_min_int(best == m ? bi : 0x7fffffff);
-      if (lane == 0) {
-        sm.rowMC[rr] = m;
-        sm.rowArg[rr] = idx;
-      }
-    } else {
-      // loads first (independent), then the online fold
-      float mc = SV_NEG_INF, s = 0.f;
-      for (int base = 0; base < a.tiles_per_row; base += 32 * 8) {
-        float2 v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = base + lane + 32 * j;
-          v[j] = i < a.tiles_per_row ? pp[i] : make_float2(SV_NEG_INF, 0.f);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (v[j].x == SV_NEG_INF) continue;
-          if (v[j].x > mc) {
-            s = s * ex2_approx(__fsub_rn(mc, v[j].x)) + v[j].y;
-            mc = v[j].x;
-          } else {
-            s += v[j].y * ex2_approx(__fsub_rn(v[j].x, mc));
-          }
-        }
-      }
-      const float M = warp_max(mc);
-      float sv = (mc == SV_NEG_INF) ? 0.f : s * ex2_approx(__fsub_rn(mc, M));
-      sv = warp_sum(sv);
-      if (lane == 0) {
-        sm.rowMC[rr] = M;
-        sm.rowS[rr] = sv;
-      }
+    const float2 st = fold_partials(a.partials + prow * a.tiles_per_row, a.tiles_per_row, greedy, lane);
+    if (lane == 0) {
+      sm.rowMC[rr] = st.x;
+      if (greedy) sm.rowArg[rr] = __float_as_int(st.y);
+      else sm.rowS[rr] = st.y;
     }
   }
 }
@@ -853,8 +900,8 @@ __device__ void fold_row_stats(const AcceptArgs& a, int b, bool greedy, AcceptSm
 // sm.bad.  With `write`, also writes accepted_len, the log-probabilities and
 // every out_tokens slot except the one a tempered row still has to sample.
 __device__ void accept_scan(const AcceptArgs& a, int b, float T, bool write, AcceptSmem& sm) {
-  const int K = a.K, lane = threadIdx.x & 31;
-  if ((threadIdx.x >> 5) != 0) return;
+  const int K = a.K, lane = gtid() & 31;
+  if ((gtid() >> 5) != 0) return;
   const bool greedy = (T == 0.f);
   const long long ob = (long long)b * (K + 1);
   const int nrows = greedy ? K + 1 : 2 * K + 1;
@@ -947,22 +994,22 @@ __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptA
   const int cs = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
   const int b = blockIdx.x / cs;
-  const int tid = threadIdx.x;
+  const int tid = gtid();
 
   // prologue: inputs only, overlaps the streaming pass
   const float T = __ldg(a.temperature + b);
   const bool greedy = (T == 0.f);
   if (rank != 0 && (greedy || !valid_temperature(T))) return;   // rank 0 alone handles these
   accept_inputs<E>(a, b, T, sm);
-  __syncthreads();
+  gsync();
   if (sm.bad && rank != 0) return;   // row-wide, so the same in every CTA of the cluster
 
   // wait for the streaming pass and the visibility of its writes
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (!sm.bad) fold_row_stats(a, b, greedy, sm);
-  __syncthreads();
+  gsync();
   accept_scan(a, b, T, rank == 0, sm);
-  __syncthreads();
+  gsync();
   if (sm.bad || greedy) return;   // the same in every CTA of the cluster
 
   // sampling at position n
@@ -976,7 +1023,7 @@ __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptA
     else sweep_slice<E, kAligned, false>(x, sm, s_part, Wt, Qt);
     cluster.sync();
     if (tid < cs) sm.recs[tid] = *cluster.map_shared_rank(&sm.rec, tid);   // one remote read each
-    __syncthreads();
+    gsync();
     if (tid == 0) decide(sm.recs, cs, residual, x.cw, u, a.groups_per_cta, sm);
     cluster.sync();   // every record has been read; shared memory may be reused
     if (sm.dec.need_p_fallback) {

@@ -45,20 +45,13 @@ def test_every_declared_symbol_is_exported(N):
 
 
 def test_workspace_bytes_arithmetic(N):
-    # at least the header, the counters and one 8-byte partial per 2 KB tile of
-    # every target and draft row, plus a 16-byte weight per 64-byte group of a row
+    # a 256-byte header, then one 8-byte partial per 2 KB tile of every target and draft row
     B, K, V = 64, 4, 128256
     tiles = -(-V // 1024)
-    groups = -(-V // 32)
-    floor = 256 + (B * (K + 1) + B * K) * tiles * 8 + B * groups * 16
-    got = N.spec_verify_workspace_bytes(B, K, V, N.SV_BF16)
-    assert floor <= got <= floor + 64 * 1024
+    assert N.spec_verify_workspace_bytes(B, K, V, N.SV_BF16) == 256 + (B * (K + 1) + B * K) * tiles * 8
     tiles32 = -(-V // 512)
-    groups32 = -(-V // 16)
-    got32 = N.spec_verify_workspace_bytes(B, K, V, N.SV_F32)
-    assert 256 + (B * (K + 1) + B * K) * tiles32 * 8 + B * groups32 * 16 <= got32
-    assert N.spec_verify_workspace_bytes(0, 4, 1000, N.SV_F32) <= 1024
-    assert N.spec_verify_workspace_bytes(8, 4, 1000, N.SV_F32) > N.spec_verify_workspace_bytes(4, 4, 1000, N.SV_F32)
+    assert N.spec_verify_workspace_bytes(B, K, V, N.SV_F32) == 256 + (B * (K + 1) + B * K) * tiles32 * 8
+    assert N.spec_verify_workspace_bytes(0, 4, 1000, N.SV_F32) == 256
     for bad in ((-1, 4, 10, 0), (1, 0, 10, 0), (1, 17, 10, 0), (1, 4, 0, 0), (1, 4, 10, 2),
                 (1, 4, N.spec_verify_max_vocab(0) + 1, 0)):
         assert N.spec_verify_workspace_bytes(*bad) == 0
@@ -123,7 +116,7 @@ def test_static_entry_point_rejects_before_touching_the_device(N):
     assert call(B=-3) == N.SV_ERR_SHAPE
     assert call(B=0) == N.SV_OK
     # the largest batch at the Llama-3 vocabulary that fits the static scratch, and one more
-    fits = [B for B in range(1, 400)
+    fits = [B for B in range(1, 4000)
             if N.spec_verify_workspace_bytes(B, 4, 128256, N.SV_BF16) <= N.SV_STATIC_SCRATCH_BYTES]
     assert fits and fits == list(range(1, fits[-1] + 1)) and fits[-1] >= 64
     assert call(B=fits[-1] + 1, V=128256) == N.SV_ERR_TOO_LARGE
