@@ -5,9 +5,7 @@
 // spec_verify_accept_sample) = two launches on the caller's stream:
 //   1. sv_row_stats_kernel, a persistent grid (SM count x resident CTAs)
 //      whose warps stream contiguous ranges of 2 KB row tiles;
-//   2. sv_accept_sample_kernel, one thread-block cluster per batch row,
-//      launched with programmatic dependent launch so its CTAs are resident
-//      and waiting when the streaming pass retires.
+//   2. sv_accept_sample_kernel, one thread-block cluster per batch row.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -232,22 +230,14 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
   cfg.blockDim = dim3(sv::kP2Threads);
   cfg.dynamicSmemBytes = accept_smem_bytes(gpc);
   cfg.stream = st;
-  cudaLaunchAttribute attrs[2];
+  cudaLaunchAttribute attrs[1];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
   attrs[0].val.clusterDim.x = (unsigned)cs;
   attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = 1;
-  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelExC(&cfg, pick_accept(dtype, aligned), args);
-  if (e != cudaSuccess) {
-    // without the early-launch overlap the dependency is plain stream order
-    (void)cudaGetLastError();
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelExC(&cfg, pick_accept(dtype, aligned), args);
-  }
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, pick_accept(dtype, aligned), args);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

@@ -134,6 +134,12 @@ __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsig
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
 // max of two packed bf16 pairs
 __device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
   uint32_t r;

@@ -44,6 +44,7 @@ constexpr int kGroupVecs = 4;                     // a sampling group: 64 B of e
 constexpr int kMaxGroupsPerThread = 8;
 constexpr int kMaxClusterSize = 16;
 constexpr int kBigCap = 1024;                     // large terms listed per sweep (more: evaluated inline)
+constexpr int kBigCapWarp = kBigCap / kP2Warps;   // each warp lists its own
 constexpr uint32_t kBigNone = 0xffffffffu;        // a claimed list slot that stays unused
 // A term whose probability exceeds this is evaluated in double-float
 // during sampling; smaller terms use the float32 path.
@@ -223,8 +224,6 @@ __device__ __forceinline__ void fold_stretch(const RowParams& rp, int ti0, int t
 template <typename E, bool kAligned>
 __global__ void __launch_bounds__(kP1Threads, 4) sv_row_stats_kernel(RowStatsArgs a) {
   if (blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0u;
-  // let the dependent accept/sample grid get scheduled early
-  asm volatile("griddepcontrol.launch_dependents;");
 
   const int lane = threadIdx.x & 31;
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -317,17 +316,16 @@ struct AcceptSmem {
   DF red[kP2Warps][4];
   int redi[kP2Warps];
   CtaRecord rec;
-  CtaRecord recs[kMaxClusterSize];
   Decision dec;
   int pick_thread;
   int pick_last;
   int group_pick;
   DF tau_group;
   DF warp_tot[kP2Warps];
-  // large terms of the current sweep: their positions ((local group << 5) |
-  // element), their double-float results (w, q), and for every (step,
-  // thread) the slice of the list its group owns ((offset << 8) | count)
-  int nbig;
+  // large terms of the current sweep, one list region per warp: their
+  // positions ((local group << 5) | element), their double-float results
+  // (w, q), and for every (step, thread) the slice of its warp's region its
+  // group owns ((offset << 8) | count)
   uint32_t bigpos[kBigCap];
   float4 bigres[kBigCap];
   uint32_t bigref[kMaxGroupsPerThread][kP2Threads];
@@ -471,21 +469,26 @@ __device__ __forceinline__ void chunk_sums(const float4* part, int ng, DF& Wt, D
 // sm.rec.  The per-thread sums of part[] over the thread's contiguous run of
 // groups come back in Wt, Qt (the locate step scans them).
 //
-// Small terms are summed in float32 as they stream by.  A large term only
-// leaves its position in a list shared by the group; once the float32 pass
-// is done, all threads evaluate the list in double-float (one term each),
-// and every thread adds the results of its own groups' terms back into
-// their weights.  A thread whose terms find the list full evaluates them
-// itself.
+// Small terms are summed in float32 as they stream by, two elements at a
+// time (paired float32 arithmetic, each lane of a pair rounded as the
+// scalar operation would be).  A large term only leaves its position in its
+// warp's list; after the float32 pass each warp evaluates its own list in
+// double-float (one term per lane) and every lane adds the results of its
+// own groups' terms back into their weights.  Terms that find the list full
+// are evaluated where they are found.
 template <typename E, bool kAligned, bool kResidual>
 __device__ void sweep_slice(const SampleCtx& x, AcceptSmem& sm, float4* part, DF& Wt, DF& Qt) {
   constexpr int kGroupElems = kGroupVecs * E::kVec;
   const int tid = gtid();
-  const int lane = tid & 31;
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t* const wpos = sm.bigpos + warp * kBigCapWarp;
+  float4* const wres = sm.bigres + warp * kBigCapWarp;
   DF accP{0.f, 0.f}, accQ{0.f, 0.f};
   int lastg = -1;
-  if (tid == 0) sm.nbig = 0;
-  gsync();
+  int wcount = 0;   // entries of this warp's list (the same in every lane)
+  const unsigned long long chi2 = f2_pack(x.c_hi, x.c_hi), clo2 = f2_pack(x.c_lo, x.c_lo);
+  const unsigned long long nmcp2 = f2_pack(-x.MCp, -x.MCp), nmcq2 = f2_pack(-x.MCq, -x.MCq);
+  const unsigned long long ncw2 = f2_pack(-x.cw, -x.cw);
   const int iters = (x.ng + kP2Threads - 1) / kP2Threads;   // the same for every thread
   for (int it = 0; it < iters; ++it) {
     const int gl = it * kP2Threads + tid;
@@ -502,32 +505,53 @@ __device__ void sweep_slice(const SampleCtx& x, AcceptSmem& sm, float4* part, DF
       if (kResidual) load_group<E, kAligned>(x.rowQ, g, x.V, wq);
     }
     // float32 pass; large terms only leave a bit in `big`
-    float sw = 0.f, sq = 0.f, sp = 0.f, sQ = 0.f;
+    unsigned long long sw2 = 0ull, sq2 = 0ull, sp2 = 0ull, sQ2 = 0ull;
     unsigned big = 0u;
 #pragma unroll
     for (int j = 0; j < kGroupVecs; ++j) {
 #pragma unroll
-      for (int k = 0; k < E::kVec; ++k) {
-        const float ep = small_exp(E::elem(wp[j], k), x.MCp, x);
+      for (int k = 0; k < E::kVec; k += 2) {
+        const unsigned long long xp2 = f2_pack(E::elem(wp[j], k), E::elem(wp[j], k + 1));
+        float ep0, ep1;
+        f2_unpack(f2_fma(xp2, clo2, f2_fma(xp2, chi2, nmcp2)), ep0, ep1);
+        ep0 = ex2_approx(ep0);
+        ep1 = ex2_approx(ep1);
+        const int bit = j * E::kVec + k;
         if (kResidual) {
-          const float eq = small_exp(E::elem(wq[j], k), x.MCq, x);
-          const bool b = ep > x.thp || eq > x.thq;
-          big |= (unsigned)b << (j * E::kVec + k);
-          const float d = b ? 0.f : __fmaf_rn(-x.cw, eq, ep);
-          sw += fmaxf(d, 0.f);
-          sq += d > 0.f ? eq : 0.f;
-          sp += b ? 0.f : ep;
-          sQ += b ? 0.f : eq;
+          const unsigned long long xq2 = f2_pack(E::elem(wq[j], k), E::elem(wq[j], k + 1));
+          float eq0, eq1;
+          f2_unpack(f2_fma(xq2, clo2, f2_fma(xq2, chi2, nmcq2)), eq0, eq1);
+          eq0 = ex2_approx(eq0);
+          eq1 = ex2_approx(eq1);
+          const bool b0 = ep0 > x.thp || eq0 > x.thq;
+          const bool b1 = ep1 > x.thp || eq1 > x.thq;
+          big |= ((unsigned)b0 << bit) | ((unsigned)b1 << (bit + 1));
+          float d0, d1;
+          f2_unpack(f2_fma(ncw2, f2_pack(eq0, eq1), f2_pack(ep0, ep1)), d0, d1);
+          d0 = b0 ? 0.f : d0;
+          d1 = b1 ? 0.f : d1;
+          sw2 = f2_add(sw2, f2_pack(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
+          sq2 = f2_add(sq2, f2_pack(d0 > 0.f ? eq0 : 0.f, d1 > 0.f ? eq1 : 0.f));
+          sp2 = f2_add(sp2, f2_pack(b0 ? 0.f : ep0, b1 ? 0.f : ep1));
+          sQ2 = f2_add(sQ2, f2_pack(b0 ? 0.f : eq0, b1 ? 0.f : eq1));
         } else {
-          const bool b = ep > x.thp;
-          big |= (unsigned)b << (j * E::kVec + k);
-          sw += b ? 0.f : ep;
+          const bool b0 = ep0 > x.thp, b1 = ep1 > x.thp;
+          big |= ((unsigned)b0 << bit) | ((unsigned)b1 << (bit + 1));
+          sw2 = f2_add(sw2, f2_pack(b0 ? 0.f : ep0, b1 ? 0.f : ep1));
         }
       }
     }
-    if (!kResidual) sp = sw;
+    float a0, a1;
+    f2_unpack(sw2, a0, a1);
+    const float sw = a0 + a1;
+    f2_unpack(sq2, a0, a1);
+    const float sq = a0 + a1;
+    f2_unpack(sp2, a0, a1);
+    const float sp = kResidual ? a0 + a1 : sw;
+    f2_unpack(sQ2, a0, a1);
+    const float sQ = a0 + a1;
     DF wg{sw, 0.f}, qg{sq, 0.f};
-    // claim list slots for this step's large terms (one atomic per warp)
+    // list this step's large terms in the warp's region
     uint32_t ref = 0;
     if (__any_sync(0xffffffffu, big != 0u)) {
       const int cnt = __popc(big);
@@ -537,24 +561,19 @@ __device__ void sweep_slice(const SampleCtx& x, AcceptSmem& sm, float4* part, DF
         const int v = __shfl_up_sync(0xffffffffu, inc, o);
         if (lane >= o) inc += v;
       }
-      int base = 0;
-      if (lane == 31) base = atomicAdd(&sm.nbig, inc);
-      base = __shfl_sync(0xffffffffu, base, 31);
       const int total = __shfl_sync(0xffffffffu, inc, 31);
-      const int off = base + inc - cnt;
-      if (base + total <= kBigCap) {
+      if (wcount + total <= kBigCapWarp) {
+        int o = wcount + inc - cnt;
+        ref = ((uint32_t)o << 8) | (uint32_t)cnt;
         unsigned m = big;
-        int o = off;
         while (m) {
           const int e = __ffs(m) - 1;
           m &= m - 1u;
-          sm.bigpos[o++] = ((uint32_t)gl << 5) | (uint32_t)e;
+          wpos[o++] = ((uint32_t)gl << 5) | (uint32_t)e;
         }
-        ref = ((uint32_t)off << 8) | (uint32_t)cnt;
+        wcount += total;
       } else {
-        // the list is full: mark this warp's claimed slots unused and
-        // evaluate the terms here
-        for (int o = off; o < off + cnt && o < kBigCap; ++o) sm.bigpos[o] = kBigNone;
+        // the list is full: evaluate the terms here
         unsigned m = big;
         while (m) {
           const int e = __ffs(m) - 1;
@@ -576,21 +595,19 @@ __device__ void sweep_slice(const SampleCtx& x, AcceptSmem& sm, float4* part, DF
     accP = df_add_f(accP, sp);
     accQ = df_add_f(accQ, sQ);
   }
-  gsync();   // the list is complete
+  __syncwarp();   // this warp's list is complete
 
-  // every listed large term, one per thread
-  const int nb = min(sm.nbig, kBigCap);
-  for (int e = tid; e < nb; e += kP2Threads) {
-    const uint32_t pos = sm.bigpos[e];
-    if (pos == kBigNone) continue;
+  // this warp's listed large terms, one per lane
+  for (int e = lane; e < wcount; e += 32) {
+    const uint32_t pos = wpos[e];
     DF w, q, ep, eq;
     big_term<E, kResidual>(x, sm.tab, ((long long)x.g0 + (pos >> 5)) * kGroupElems + (pos & 31u), w,
                            q, ep, eq);
-    sm.bigres[e] = make_float4(w.hi, w.lo, q.hi, q.lo);
-    accP = df_add(accP, ep);   // the totals do not care which thread adds them
+    wres[e] = make_float4(w.hi, w.lo, q.hi, q.lo);
+    accP = df_add(accP, ep);   // the totals do not care which lane adds them
     accQ = df_add(accQ, eq);
   }
-  gsync();
+  __syncwarp();
 
   // fold the results back into the groups that own them
   for (int it = 0; it < iters; ++it) {
@@ -601,7 +618,7 @@ __device__ void sweep_slice(const SampleCtx& x, AcceptSmem& sm, float4* part, DF
     float4 p4 = part[gl];
     DF wg{p4.x, p4.y}, qg{p4.z, p4.w};
     for (int o = (int)(ref >> 8); o < (int)(ref >> 8) + cnt; ++o) {
-      const float4 r = sm.bigres[o];
+      const float4 r = wres[o];
       wg = df_add(wg, DF{r.x, r.y});
       qg = df_add(qg, DF{r.z, r.w});
     }
@@ -624,51 +641,52 @@ __device__ void sweep_slice(const SampleCtx& x, AcceptSmem& sm, float4* part, DF
   }
 }
 
-// Thread 0 of every CTA: combine the cluster's records (already copied
-// into recs[] by threads 0..cs-1) into the decision.  Every CTA reads the
-// same records in the same order, so all agree.
-__device__ void decide(const CtaRecord* recs, int cs, bool residual, float cw, float u,
+// Warp 0 of every CTA: combine the cluster's records into the decision.
+// Lane r holds record r (lanes from cs on hold nothing).  Every CTA runs the
+// same lanes on the same records, so all agree.
+__device__ void decide(const CtaRecord& rec, int cs, bool residual, float cw, float u,
                        int groups_per_cta, AcceptSmem& sm) {
-  DF Sp{0.f, 0.f}, Sq{0.f, 0.f}, tot{0.f, 0.f};
-  int last_group = -1;
-  for (int r = 0; r < cs; ++r) {
-    Sp = df_add(Sp, recs[r].Sp);
-    Sq = df_add(Sq, recs[r].Sq);
-    last_group = max(last_group, recs[r].last_group);
-  }
-  DF dc{0.f, 0.f};
+  const int lane = gtid() & 31;
+  const bool have = lane < cs;
+  const DF zero{0.f, 0.f};
+  const DF Sp = warp_sum_df(have ? rec.Sp : zero);
+  const DF Sq = warp_sum_df(have ? rec.Sq : zero);
+  int last_group = have ? rec.last_group : -1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) last_group = max(last_group, __shfl_xor_sync(0xffffffffu, last_group, o));
+  DF dc = zero;
   if (residual) dc = df_sub(df_div(Sp, Sq), DF{cw, 0.f});
-  DF wr[kMaxClusterSize];
-  for (int r = 0; r < cs; ++r) {
-    wr[r] = residual ? df_sub(recs[r].W, df_mul(dc, recs[r].Q)) : recs[r].W;
-    tot = df_add(tot, wr[r]);
+  const DF wr = !have ? zero : (residual ? df_sub(rec.W, df_mul(dc, rec.Q)) : rec.W);
+  // inclusive and exclusive prefix sums of the corrected CTA weights
+  DF inc = wr;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF up = df_shfl_up(inc, o);
+    if (lane >= o) inc = df_add(inc, up);
   }
+  DF exc = df_shfl_up(inc, 1);
+  if (lane == 0) exc = zero;
+  const DF tot{__shfl_sync(0xffffffffu, inc.hi, 31), __shfl_sync(0xffffffffu, inc.lo, 31)};
   Decision d;
   d.dc = dc;
   d.last_group = last_group;
   d.need_p_fallback = residual && !df_pos(tot);
   d.fallback_last = 0;
   d.rstar = -1;
-  d.tau_local = DF{0.f, 0.f};
-  if (!d.need_p_fallback) {
-    // tau = u * W: the token is the smallest index whose prefix exceeds tau
-    const DF tau = df_mul_f(tot, u);
-    DF pre{0.f, 0.f};
-    for (int r = 0; r < cs; ++r) {
-      const DF nxt = df_add(pre, wr[r]);
-      if (df_pos(wr[r]) && df_lt(tau, nxt)) {
-        d.rstar = r;
-        d.tau_local = df_sub(tau, pre);
-        break;
-      }
-      pre = nxt;
-    }
-    if (d.rstar < 0) {
-      d.fallback_last = 1;
-      d.rstar = last_group >= 0 ? last_group / groups_per_cta : 0;
-    }
+  d.tau_local = zero;
+  // tau = u * W: the token is the smallest index whose prefix exceeds tau
+  const DF tau = df_mul_f(tot, u);
+  const unsigned hit = __ballot_sync(0xffffffffu, have && df_pos(wr) && df_lt(tau, inc));
+  const DF tl = df_sub(tau, exc);
+  if (hit) {
+    d.rstar = __ffs(hit) - 1;
+    d.tau_local = DF{__shfl_sync(0xffffffffu, tl.hi, d.rstar), __shfl_sync(0xffffffffu, tl.lo, d.rstar)};
   }
-  sm.dec = d;
+  if (!d.need_p_fallback && d.rstar < 0) {
+    d.fallback_last = 1;
+    d.rstar = last_group >= 0 ? last_group / groups_per_cta : 0;
+  }
+  if (lane == 0) sm.dec = d;
 }
 
 // Find the token inside CTA rstar (all threads of that CTA).
@@ -824,23 +842,49 @@ __device__ void accept_inputs(const AcceptArgs& a, int b, float T, AcceptSmem& s
     for (int i = gtid(); i < 256; i += kP2Threads) sm.tab[i] = kExp2Table256[i];
 }
 
-// One warp folds the tpr tile partials of one row: (MC, S) for a tempered
-// row, (max logit, lowest index holding it as int bits) for a greedy row
-// (whose partials hold the complemented index).  Every lane returns the
-// result.
+// Reductions over aligned groups of kLanes lanes (kLanes = 16 or 32); every
+// lane of the warp takes part, each group reduces on its own.
+template <int kLanes>
+__device__ __forceinline__ float grp_max(float v) {
+#pragma unroll
+  for (int o = kLanes / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+template <int kLanes>
+__device__ __forceinline__ float grp_sum(float v) {
+#pragma unroll
+  for (int o = kLanes / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+template <int kLanes>
+__device__ __forceinline__ int grp_min_int(int v) {
+#pragma unroll
+  for (int o = kLanes / 2; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// A group of kLanes lanes (lane = index in the group) folds the tpr tile
+// partials of one row: (MC, S) for a tempered row, (max logit, lowest index
+// holding it as int bits) for a greedy row (whose partials hold the
+// complemented index).  Every lane of the group returns the result.  With
+// pp == nullptr the group folds nothing and returns the neutral values (it
+// still takes part in the shuffles).
+template <int kLanes>
 __device__ __forceinline__ float2 fold_partials(const float2* pp, int tpr, bool greedy, int lane) {
+  constexpr int kPer = 8;   // partials in flight per lane
+  const int n = pp ? tpr : 0;
   if (greedy) {
     float best = SV_NEG_INF;
     int bi = 0x7fffffff;
-    for (int base = 0; base < tpr; base += 32 * 8) {
-      float2 v[8];
+    for (int base = 0; base < n; base += kLanes * kPer) {
+      float2 v[kPer];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = base + lane + 32 * j;
-        v[j] = i < tpr ? __ldcg(pp + i) : make_float2(SV_NEG_INF, __int_as_float(~0x7fffffff));
+      for (int j = 0; j < kPer; ++j) {
+        const int i = base + lane + kLanes * j;
+        v[j] = i < n ? __ldcg(pp + i) : make_float2(SV_NEG_INF, __int_as_float(~0x7fffffff));
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < kPer; ++j) {
         const int idx = ~__float_as_int(v[j].y);
         if (v[j].x > best || (v[j].x == best && idx < bi)) {
           best = v[j].x;
@@ -848,21 +892,21 @@ __device__ __forceinline__ float2 fold_partials(const float2* pp, int tpr, bool 
         }
       }
     }
-    const float m = warp_max(best);
-    const int idx = warp_min_int(best == m ? bi : 0x7fffffff);
+    const float m = grp_max<kLanes>(best);
+    const int idx = grp_min_int<kLanes>(best == m ? bi : 0x7fffffff);
     return make_float2(m, __int_as_float(idx));
   }
   // loads first (independent), then the online fold
   float mc = SV_NEG_INF, s = 0.f;
-  for (int base = 0; base < tpr; base += 32 * 8) {
-    float2 v[8];
+  for (int base = 0; base < n; base += kLanes * kPer) {
+    float2 v[kPer];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = base + lane + 32 * j;
-      v[j] = i < tpr ? __ldcg(pp + i) : make_float2(SV_NEG_INF, 0.f);
+    for (int j = 0; j < kPer; ++j) {
+      const int i = base + lane + kLanes * j;
+      v[j] = i < n ? __ldcg(pp + i) : make_float2(SV_NEG_INF, 0.f);
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kPer; ++j) {
       if (v[j].x == SV_NEG_INF) continue;
       if (v[j].x > mc) {
         s = s * ex2_approx(__fsub_rn(mc, v[j].x)) + v[j].y;
@@ -872,23 +916,30 @@ __device__ __forceinline__ float2 fold_partials(const float2* pp, int tpr, bool 
       }
     }
   }
-  const float M = warp_max(mc);
+  const float M = grp_max<kLanes>(mc);
   float sv = (mc == SV_NEG_INF) ? 0.f : s * ex2_approx(__fsub_rn(mc, M));
-  sv = warp_sum(sv);
+  sv = grp_sum<kLanes>(sv);
   return make_float2(M, sv);
 }
 
-// Fold the tile partials of batch row b into row statistics, one warp per
-// row: (MC, S) for tempered rows, (max, lowest argmax) for greedy rows.
+// Fold the tile partials of batch row b into row statistics, one half-warp
+// per row (16 rows per round): (MC, S) for tempered rows, (max, lowest
+// argmax) for greedy rows.
 __device__ void fold_row_stats(const AcceptArgs& a, int b, bool greedy, AcceptSmem& sm) {
-  const int K = a.K, lane = gtid() & 31, warp = gtid() >> 5;
+  constexpr int kHalves = kP2Threads / 16;
+  const int K = a.K, hl = gtid() & 15, hw = gtid() >> 4;
   const long long tb = (long long)b * (K + 1);
   const long long db = a.n_target_rows + (long long)b * K;
   const int nrows = greedy ? K + 1 : 2 * K + 1;
-  for (int rr = warp; rr < nrows; rr += kP2Warps) {
-    const long long prow = (rr <= K) ? tb + rr : db + (rr - K - 1);
-    const float2 st = fold_partials(a.partials + prow * a.tiles_per_row, a.tiles_per_row, greedy, lane);
-    if (lane == 0) {
+  for (int base = 0; base < nrows; base += kHalves) {   // the same trip count in every warp
+    const int rr = base + hw;
+    const float2* pp = nullptr;
+    if (rr < nrows) {
+      const long long prow = (rr <= K) ? tb + rr : db + (rr - K - 1);
+      pp = a.partials + prow * a.tiles_per_row;
+    }
+    const float2 st = fold_partials<16>(pp, a.tiles_per_row, greedy, hl);
+    if (pp && hl == 0) {
       sm.rowMC[rr] = st.x;
       if (greedy) sm.rowArg[rr] = __float_as_int(st.y);
       else sm.rowS[rr] = st.y;
@@ -996,7 +1047,7 @@ __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptA
   const int b = blockIdx.x / cs;
   const int tid = gtid();
 
-  // prologue: inputs only, overlaps the streaming pass
+  // inputs only
   const float T = __ldg(a.temperature + b);
   const bool greedy = (T == 0.f);
   if (rank != 0 && (greedy || !valid_temperature(T))) return;   // rank 0 alone handles these
@@ -1004,8 +1055,6 @@ __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptA
   gsync();
   if (sm.bad && rank != 0) return;   // row-wide, so the same in every CTA of the cluster
 
-  // wait for the streaming pass and the visibility of its writes
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (!sm.bad) fold_row_stats(a, b, greedy, sm);
   gsync();
   accept_scan(a, b, T, rank == 0, sm);
@@ -1022,9 +1071,11 @@ __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptA
     if (residual) sweep_slice<E, kAligned, true>(x, sm, s_part, Wt, Qt);
     else sweep_slice<E, kAligned, false>(x, sm, s_part, Wt, Qt);
     cluster.sync();
-    if (tid < cs) sm.recs[tid] = *cluster.map_shared_rank(&sm.rec, tid);   // one remote read each
-    gsync();
-    if (tid == 0) decide(sm.recs, cs, residual, x.cw, u, a.groups_per_cta, sm);
+    if (tid < 32) {   // warp 0: one remote record per lane, then the decision
+      CtaRecord rec{};
+      if (tid < cs) rec = *cluster.map_shared_rank(&sm.rec, tid);
+      decide(rec, cs, residual, x.cw, u, a.groups_per_cta, sm);
+    }
     cluster.sync();   // every record has been read; shared memory may be reused
     if (sm.dec.need_p_fallback) {
       residual = false;   // the residual is zero everywhere: draw from p_t instead
