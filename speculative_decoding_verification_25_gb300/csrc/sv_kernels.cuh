@@ -313,7 +313,6 @@ struct AcceptSmem {
   float xq[kMaxK];
   int bad;
   int n;
-  DF red[kP2Warps][4];
   int redi[kP2Warps];
   CtaRecord rec;
   Decision dec;
@@ -386,34 +385,37 @@ __device__ __forceinline__ void eval_pair(float xp, float xq, const SampleCtx& s
 }
 
 // Block-wide sum of four double-floats; every thread gets the totals.
-__device__ __forceinline__ void block_sum4(DF (&v)[4], AcceptSmem& sm) {
-  const int lane = gtid() & 31, warp = gtid() >> 5;
+// Block totals of four double-floats and the block maximum of an int (at
+// least -1); every thread gets them.  Each thread leaves its values in the
+// large-term lists (free once a sweep has folded them back), warps 0..3 sum
+// one column each and warp 4 takes the maximum.
+__device__ __forceinline__ void block_totals(DF (&v)[4], int& imax, AcceptSmem& sm) {
+  static_assert(4 * kP2Threads * sizeof(DF) <= sizeof(sm.bigres), "scratch for the columns");
+  static_assert(kP2Threads * sizeof(int) <= sizeof(sm.bigpos), "scratch for the maxima");
+  static_assert(kP2Warps >= 5, "five reducing warps");
+  const int tid = gtid(), lane = tid & 31, warp = tid >> 5;
+  DF* col = reinterpret_cast<DF*>(sm.bigres);
+  int* icol = reinterpret_cast<int*>(sm.bigpos);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = warp_sum_df(v[i]);
-  if (lane == 0)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sm.red[warp][i] = v[i];
+  for (int i = 0; i < 4; ++i) col[i * kP2Threads + tid] = v[i];
+  icol[tid] = imax;
   gsync();
-  if (gtid() < 4) {
+  if (warp < 4) {
     DF t{0.f, 0.f};
-    for (int w = 0; w < kP2Warps; ++w) t = df_add(t, sm.red[w][gtid()]);
-    sm.red1[gtid()] = t;
+    for (int k = lane; k < kP2Threads; k += 32) t = df_add(t, col[warp * kP2Threads + k]);
+    t = warp_sum_df(t);
+    if (lane == 0) sm.red1[warp] = t;
+  } else if (warp == 4) {
+    int m = -1;
+    for (int k = lane; k < kP2Threads; k += 32) m = max(m, icol[k]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) sm.redi[0] = m;
   }
   gsync();
 #pragma unroll
   for (int i = 0; i < 4; ++i) v[i] = sm.red1[i];
-}
-
-__device__ __forceinline__ int block_max_int(int v, AcceptSmem& sm) {
-  const int lane = gtid() & 31, warp = gtid() >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if (lane == 0) sm.redi[warp] = v;
-  gsync();
-  int t = sm.redi[0];
-  for (int w = 1; w < kP2Warps; ++w) t = max(t, sm.redi[w]);
-  gsync();
-  return t;
+  imax = sm.redi[0];
 }
 
 // Load group g (kGroupVecs vectors) of a row.
@@ -629,8 +631,8 @@ __device__ void sweep_slice(const SampleCtx& x, AcceptSmem& sm, float4* part, DF
 
   chunk_sums(part, x.ng, Wt, Qt);
   DF tot[4] = {Wt, Qt, accP, accQ};
-  block_sum4(tot, sm);
-  const int last = block_max_int(lastg, sm);
+  int last = lastg;
+  block_totals(tot, last, sm);
   if (tid == 0) {
     sm.rec.W = tot[0];
     sm.rec.Q = tot[1];
