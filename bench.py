@@ -371,16 +371,7 @@ def run_ours(args):
     hbm, peak_src = peaks()
     k1_gbs = p1_bytes / (k1_ms * 1e-3) / 1e9
     step_gbs = (p1_bytes + p2_bytes) / (ms_per_step * 1e-3) / 1e9
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "row_stats_traffic.json")
-    if os.path.exists(tr_path):
-        try:
-            with open(tr_path) as f:
-                tr = json.load(f)
-            if tr.get("workload") == args.workload and tr.get("kernel_rev") == kernel_rev():
-                traffic = tr.get("bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = stored_traffic(args.workload)
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
@@ -417,16 +408,43 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def kernel_rev():
-    """Hash of the kernel sources: a stored ncu traffic figure is used only
-    while the kernels it was taken on are unchanged."""
+def stored_traffic(workload):
+    """DRAM bytes per launch of the streaming kernel from the committed ncu
+    summary of this workload, or None when the summary was taken on other
+    kernel sources (or is missing)."""
+    path = os.path.join(ROOT, "profiles", f"sv_row_stats_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip()
+    if fields.get("kernel_rev") != kernel_rev():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# the sources each kernel is built from (a stored ncu figure applies while
+# they are unchanged)
+KERNEL_SOURCES = {
+    "sv_row_stats_kernel": ("sv_common.cuh", "sv_stream.cuh"),
+    "sv_accept_sample_kernel": ("sv_common.cuh", "sv_stream.cuh", "sv_sample.cuh", "exp2_table.inc"),
+}
+
+
+def kernel_rev(kernel="sv_row_stats_kernel"):
+    """Hash of one kernel's sources."""
     import hashlib
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_25_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".inc")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:12]
 
 

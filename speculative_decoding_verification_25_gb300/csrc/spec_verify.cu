@@ -14,7 +14,7 @@
 #include <mutex>
 
 #include "spec_verify.h"
-#include "sv_kernels.cuh"
+#include "sv_sample.cuh"
 
 namespace {
 

@@ -61,3 +61,24 @@ def test_reference_arm_prints_one_json_line():
     line = json.loads(res.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_stored_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    # the hash is taken over the real sources; only the summary file is fake
+    rev = bench.kernel_rev("sv_row_stats_kernel")
+    (prof / "sv_row_stats_kernel_w.md").write_text(
+        f"# x\n\n- kernel_rev: {rev}\n- dram_bytes_per_launch: 12345\n")
+    (prof / "sv_row_stats_kernel_old.md").write_text(
+        "- kernel_rev: 000000000000\n- dram_bytes_per_launch: 999\n")
+    real_root = bench.ROOT
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_rev", lambda kernel="sv_row_stats_kernel": rev)
+    assert bench.stored_traffic("w") == 12345
+    assert bench.stored_traffic("old") is None        # taken on other sources
+    assert bench.stored_traffic("missing") is None
+    monkeypatch.setattr(bench, "ROOT", real_root)
+    assert set(bench.KERNEL_SOURCES) == {"sv_row_stats_kernel", "sv_accept_sample_kernel"}
