@@ -28,7 +28,6 @@ constexpr int kTileVecsPerLane = 4;               // 4 x 16 B per lane
 constexpr int kTileVecs = 32 * kTileVecsPerLane;  // one 2 KB tile of one row
 constexpr int kP1Threads = 256;
 
-
 struct RowStatsArgs {
   const void* target;
   const void* draft;
@@ -44,13 +43,6 @@ struct RowStatsArgs {
 // float32 c = log2(e)/T, the same in both kernels
 __device__ __forceinline__ float log2e_over_f(float T) { return __fdiv_rn(kLog2eHi, T); }
 
-// Row `row` of the stacked [target rows; draft rows] and its batch row.
-__device__ __forceinline__ void row_info(const RowStatsArgs& a, int row, int& b, bool& is_draft,
-                                         int& r) {
-  is_draft = row >= a.n_target_rows;
-  r = is_draft ? row - a.n_target_rows : row;
-  b = is_draft ? r / a.K : r / (a.K + 1);
-}
 
 // ============================================================== streaming pass
 // One tile of one lane: kTileVecsPerLane 16-byte vectors, 512 bytes apart.
@@ -120,24 +112,31 @@ __device__ __forceinline__ void fold_tile(const uint32_t (&w)[kTileVecsPerLane][
 #pragma unroll
       for (int i = 0; i < 4; ++i) m = fmaxf(m, __uint_as_float(w[j][i]));
   }
-  if (m == SV_NEG_INF) return;
+  // new lane shift (no branches): a tile whose max is not above the shift
+  // leaves it and the sum as they are; an all -inf tile adds zeros
   const float tmc = __fmul_rn(m, c);
-  if (tmc > st.mc) {   // new lane shift: rescale what was summed so far
-    st.s *= ex2_approx(__fsub_rn(st.mc, tmc));
-    st.mc = tmc;
-  }
-  const float nmc = -st.mc;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  const float mc1 = fmaxf(st.mc, tmc);
+  st.s *= (mc1 == st.mc) ? 1.f : ex2_approx(__fsub_rn(st.mc, mc1));
+  st.mc = mc1;
+  const float nmc = (mc1 == SV_NEG_INF) ? 0.f : -mc1;
+  // four running sums (elements k mod 4), two per paired instruction; each
+  // half rounds as the scalar FFMA / FADD would
+  const unsigned long long c2 = f2_pack(c, c), nmc2 = f2_pack(nmc, nmc);
+  unsigned long long s01 = 0ull, s23 = 0ull;
 #pragma unroll
   for (int j = 0; j < kTileVecsPerLane; ++j) {
 #pragma unroll
     for (int k = 0; k < E::kVec; k += 4) {
-      a0 += ex2_approx(__fmaf_rn(E::elem(w[j], k + 0), c, nmc));
-      a1 += ex2_approx(__fmaf_rn(E::elem(w[j], k + 1), c, nmc));
-      a2 += ex2_approx(__fmaf_rn(E::elem(w[j], k + 2), c, nmc));
-      a3 += ex2_approx(__fmaf_rn(E::elem(w[j], k + 3), c, nmc));
+      float y0, y1, y2, y3;
+      f2_unpack(f2_fma(f2_pack(E::elem(w[j], k + 0), E::elem(w[j], k + 1)), c2, nmc2), y0, y1);
+      f2_unpack(f2_fma(f2_pack(E::elem(w[j], k + 2), E::elem(w[j], k + 3)), c2, nmc2), y2, y3);
+      s01 = f2_add(s01, f2_pack(ex2_approx(y0), ex2_approx(y1)));
+      s23 = f2_add(s23, f2_pack(ex2_approx(y2), ex2_approx(y3)));
     }
   }
+  float a0, a1, a2, a3;
+  f2_unpack(s01, a0, a1);
+  f2_unpack(s23, a2, a3);
   st.s += (a0 + a1) + (a2 + a3);
 }
 
@@ -160,38 +159,100 @@ __device__ __forceinline__ void flush_stretch(float2* pp, int first, int last, b
   for (int k = first + lane; k <= last; k += 32) pp[k] = (k == last) ? part : neutral;
 }
 
-// Parameters of one row of the stacked [target rows; draft rows].
-struct RowParams {
-  bool active, greedy;
-  float c;
-  const char* rowp;
-  RowParams() = default;
-  __device__ __forceinline__ RowParams(const RowStatsArgs& a, int row, int elem_bytes) {
-    int b, r;
-    bool is_draft;
-    row_info(a, row, b, is_draft, r);
-    const float T = __ldg(a.temperature + b);
-    greedy = (T == 0.f);
-    active = valid_temperature(T) && !(is_draft && greedy);
-    c = greedy ? 0.f : log2e_over_f(T);
-    rowp = (const char*)(is_draft ? a.draft : a.target) + (long long)r * a.V * elem_bytes;
+// Everything a warp needs about the rows its range touches.  Lane i holds
+// the temperature of the range's i-th row; later rows (ranges over 32 rows
+// long, tiny vocabularies only) read theirs when they are reached.
+struct WarpRows {
+  const RowStatsArgs* a;
+  long long t1;        // end of the range (stacked tile index)
+  int row0;            // first row of the range
+  float T_lane;
+  unsigned act_mask;   // bit i: row row0 + i is read (i < 32)
+
+  __device__ __forceinline__ int batch_of(int row) const {
+    return row < a->n_target_rows ? row / (a->K + 1) : (row - a->n_target_rows) / a->K;
+  }
+  __device__ __forceinline__ float T_of(int row) const {   // warp-uniform call
+    const int d = row - row0;
+    const float t = __shfl_sync(0xffffffffu, T_lane, d & 31);
+    return d < 32 ? t : __ldg(a->temperature + batch_of(row));
+  }
+  __device__ __forceinline__ bool row_read(int row, float T) const {
+    return valid_temperature(T) && !(row >= a->n_target_rows && T == 0.f);
+  }
+  __device__ __forceinline__ bool active(int row) const {   // warp-uniform call
+    const int d = row - row0;
+    return d < 32 ? ((act_mask >> d) & 1u) != 0u : row_read(row, T_of(row));
+  }
+  __device__ __forceinline__ const char* rowp(int row, int elem_bytes) const {
+    const bool d = row >= a->n_target_rows;
+    const long long r = d ? row - a->n_target_rows : row;
+    return (const char*)(d ? a->draft : a->target) + r * a->V * elem_bytes;
   }
 };
 
-// Fold tiles [ti0, ti1) of one row into `st`, two tiles per trip with the
-// next tile's loads in flight while the current one is folded.
-template <typename E, bool kAligned, bool kGreedy>
-__device__ __forceinline__ void fold_stretch(const RowParams& rp, int ti0, int ti1, int lane, int V,
-                                             int full_end, LaneStats& st) {
-  uint32_t wa[kTileVecsPerLane][4], wb[kTileVecsPerLane][4];
-  load_tile<E, kAligned>(wa, rp.rowp, ti0, lane, V, ti0 < full_end, true);
-  for (int ti = ti0; ti < ti1; ti += 2) {
-    const bool has1 = ti + 1 < ti1;
-    if (has1) load_tile<E, kAligned>(wb, rp.rowp, ti + 1, lane, V, ti + 1 < full_end, true);
-    fold_tile<E>(wa, (long long)ti * kTileVecs + lane, kGreedy, rp.c, st);
-    if (!has1) break;
-    if (ti + 2 < ti1) load_tile<E, kAligned>(wa, rp.rowp, ti + 2, lane, V, ti + 2 < full_end, true);
-    fold_tile<E>(wb, (long long)(ti + 1) * kTileVecs + lane, kGreedy, rp.c, st);
+// A position in a warp's range: stacked tile index t, its row and its tile
+// within the row (kept in step without divisions).
+struct TilePos {
+  long long t;
+  int row, ti;
+  // move forward to the first tile of an active row at or after this one
+  // (t = t1 if there is none)
+  __device__ __forceinline__ void settle(const WarpRows& wr) {
+    const int tpr = wr.a->tiles_per_row;
+    while (t < wr.t1 && !wr.active(row)) {
+      t += tpr - ti;
+      ti = 0;
+      ++row;
+    }
+    if (t > wr.t1) t = wr.t1;
+  }
+  __device__ __forceinline__ TilePos next(const WarpRows& wr) const {
+    TilePos p = *this;
+    ++p.t;
+    if (++p.ti == wr.a->tiles_per_row) {
+      p.ti = 0;
+      ++p.row;
+    }
+    p.settle(wr);
+    return p;
+  }
+};
+
+// The open row stretch of a warp: which row, its first tile, its parameters.
+struct Stretch {
+  int row, first;
+  bool greedy;
+  float c;
+  LaneStats st;
+  __device__ __forceinline__ void open(const WarpRows& wr, int r, int ti) {
+    row = r;
+    first = ti;
+    const float T = wr.T_of(r);
+    greedy = (T == 0.f);
+    c = greedy ? 0.f : log2e_over_f(T);
+    st.reset();
+  }
+};
+
+template <typename E, bool kAligned>
+__device__ __forceinline__ void load_at(uint32_t (&w)[kTileVecsPerLane][4], const WarpRows& wr,
+                                        const TilePos& p, int lane, int full_end) {
+  load_tile<E, kAligned>(w, wr.rowp(p.row, E::kBytes), p.ti, lane, wr.a->V, p.ti < full_end, true);
+}
+
+// Fold the tile at t (its data in w) into the open stretch; if the next tile
+// `nt` of the sequence is in another row (or past the end), write the
+// stretch's partials and open the next one.
+template <typename E>
+__device__ __forceinline__ void fold_at(const uint32_t (&w)[kTileVecsPerLane][4], const WarpRows& wr,
+                                        const TilePos& p, const TilePos& np, int lane, Stretch& sr) {
+  fold_tile<E>(w, (long long)p.ti * kTileVecs + lane, sr.greedy, sr.c, sr.st);
+  const bool more = np.t < wr.t1;
+  if (!more || np.row != p.row) {
+    flush_stretch(wr.a->partials + (long long)p.row * wr.a->tiles_per_row, sr.first, p.ti, sr.greedy,
+                  lane, sr.st);
+    if (more) sr.open(wr, np.row, np.ti);
   }
 }
 
@@ -204,24 +265,44 @@ __global__ void __launch_bounds__(kP1Threads, 4) sv_row_stats_kernel(RowStatsArg
   const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
   const long long t0 = gw * a.n_tiles / nw;
   const long long t1 = (gw + 1) * a.n_tiles / nw;
+  if (t0 >= t1) return;
   const int tpr = a.tiles_per_row;
   // tiles below full_end lie wholly inside the row (the last one may be ragged)
   const int full_end = ((long long)tpr * kTileVecs * E::kVec == a.V) ? tpr : tpr - 1;
 
-  // the warp's range crosses a few rows: one stretch per row
-  for (long long tile = t0; tile < t1;) {
-    const int row = (int)(tile / tpr);
-    const int ti0 = (int)(tile - (long long)row * tpr);
-    const int ti1 = (int)min((long long)tpr, ti0 + (t1 - tile));
-    const RowParams rp(a, row, E::kBytes);
-    if (rp.active) {
-      LaneStats st;
-      st.reset();
-      if (rp.greedy) fold_stretch<E, kAligned, true>(rp, ti0, ti1, lane, a.V, full_end, st);
-      else fold_stretch<E, kAligned, false>(rp, ti0, ti1, lane, a.V, full_end, st);
-      flush_stretch(a.partials + (long long)row * tpr, ti0, ti1 - 1, rp.greedy, lane, st);
-    }
-    tile += ti1 - ti0;
+  WarpRows wr;
+  wr.a = &a;
+  wr.t1 = t1;
+  wr.row0 = (int)(t0 / tpr);
+  TilePos pa;
+  pa.t = t0;
+  pa.row = wr.row0;
+  pa.ti = (int)(t0 - (long long)wr.row0 * tpr);
+  // the first tile's loads go out before the row's temperature is known
+  // (they are repeated elsewhere in the rare case its row is not read)
+  uint32_t wa[kTileVecsPerLane][4], wb[kTileVecsPerLane][4];
+  load_at<E, kAligned>(wa, wr, pa, lane, full_end);
+  const int row_last = (int)((t1 - 1) / tpr);
+  wr.T_lane = (wr.row0 + lane <= row_last) ? __ldg(a.temperature + wr.batch_of(wr.row0 + lane)) : 0.f;
+  wr.act_mask = __ballot_sync(0xffffffffu, wr.row0 + lane <= row_last && wr.row_read(wr.row0 + lane, wr.T_lane));
+
+  // one register ping-pong over the warp's active tiles, across row
+  // boundaries: the next tile's loads are always in flight while the
+  // current one is folded
+  pa.settle(wr);
+  if (pa.t >= t1) return;
+  if (pa.t != t0) load_at<E, kAligned>(wa, wr, pa, lane, full_end);
+  Stretch sr;
+  sr.open(wr, pa.row, pa.ti);
+  for (;;) {
+    const TilePos pb = pa.next(wr);
+    if (pb.t < t1) load_at<E, kAligned>(wb, wr, pb, lane, full_end);
+    fold_at<E>(wa, wr, pa, pb, lane, sr);
+    if (pb.t >= t1) break;
+    pa = pb.next(wr);
+    if (pa.t < t1) load_at<E, kAligned>(wa, wr, pa, lane, full_end);
+    fold_at<E>(wb, wr, pb, pa, lane, sr);
+    if (pa.t >= t1) break;
   }
 }
 
