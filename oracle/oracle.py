@@ -64,6 +64,9 @@ R10 A row whose temperature is negative, NaN, infinite or a nonzero value
     accepted_len = -1 and every out_tokens slot is -1.
 R11 Logits may be -inf (probability 0); NaN and +inf are outside the
     contract (this oracle raises on them).
+R13 Adaptive verification (spec_verify_ragged): row b with K_b drafted
+    tokens is the fixed-K rule on its prefix, with u = uniforms[b, K_b];
+    K_b outside [0, K] makes an error row.
 """
 from __future__ import annotations
 
@@ -180,7 +183,8 @@ def verify_row(target: np.ndarray, draft: np.ndarray, tokens: np.ndarray,
         return _error_row(K)
 
     logP = np.stack([log_softmax(target[t], T) for t in range(K + 1)])
-    logQ = np.stack([log_softmax(draft[t], T) for t in range(K)])
+    logQ = (np.stack([log_softmax(draft[t], T) for t in range(K)]) if K else
+            np.empty((0, V)))
     return accept_and_sample(logP, logQ, tokens, uniforms)
 
 
@@ -262,6 +266,53 @@ def spec_verify(target_logits, draft_logits, draft_tokens, uniforms, temperature
                          float(temperature[b]))
         al[b], ot[b], lp[b], lq[b] = res.accepted_len, res.out_tokens, res.logp, res.logq
         rm[b], cm[b] = res.ratio_margin, res.cdf_margin
+        modes.append(res.mode)
+    return BatchResult(al, ot, lp, lq, rm, cm, modes)
+
+
+def spec_verify_ragged(target_logits, draft_logits, draft_tokens, uniforms, temperature,
+                       k_per_row, dtype: str | None = None) -> BatchResult:
+    """Adaptive verification: row b verifies only its first K_b drafted
+    tokens, 0 <= K_b <= K.  The stream transcript "IA local 202: acelere
+    muito a geração com speculative decoding" (44:15-45:16, "adaptive
+    verification") describes validating a different number of drafted
+    tokens per request.
+
+    Reading R13: row b is the fixed-K rule on its prefix -- target rows
+    0..K_b, draft rows 0..K_b-1, tokens x_0..x_{K_b-1}, acceptance draws
+    r_0..r_{K_b-1} and the replacement/bonus draw u = uniforms[b, K_b]
+    (the column right after its own draws).  Outputs keep the padded K
+    layout: out_tokens slots after the emitted ones are -1 and the
+    log-probabilities of positions K_b..K-1 are NaN.  K_b outside [0, K]
+    makes an error row (reading R10's convention).
+    """
+    B = len(temperature)
+    K = np.asarray(draft_tokens).shape[1]
+    k_per_row = np.asarray(k_per_row)
+    al = np.empty(B, np.int32)
+    ot = np.full((B, K + 1), -1, np.int32)
+    lp = np.full((B, K), np.nan)
+    lq = np.full((B, K), np.nan)
+    rm = np.full((B, K), np.inf)
+    cm = np.full(B, np.inf)
+    modes = []
+    for b in range(B):
+        kb = int(k_per_row[b])
+        if kb < 0 or kb > K:
+            al[b] = -1
+            modes.append("error")
+            continue
+        tg = target_logits[b][:kb + 1]
+        dr = draft_logits[b][:kb]
+        if dtype is not None:
+            tg = decode_logits(tg, dtype)
+            dr = decode_logits(dr, dtype)
+        unif = np.asarray(uniforms[b])[:kb + 1]
+        res = verify_row(tg, dr, np.asarray(draft_tokens[b])[:kb], unif, float(temperature[b]))
+        al[b] = res.accepted_len
+        ot[b, :kb + 1] = res.out_tokens
+        lp[b, :kb], lq[b, :kb] = res.logp, res.logq
+        rm[b, :kb], cm[b] = res.ratio_margin, res.cdf_margin
         modes.append(res.mode)
     return BatchResult(al, ot, lp, lq, rm, cm, modes)
 

@@ -30,6 +30,8 @@ without generating the rest):
 * uniforms are 24-bit integers times 2**-24, so every float32 value lies in
   [0, 1) exactly.  Column t < K is the acceptance draw r_t of position t,
   column K is the single draw u used for the replacement or bonus token.
+* the ragged workload also draws, per batch row, how many drafted tokens
+  the row verifies: K_b uniform in {0, ..., K} (its draw u is column K_b).
 """
 from __future__ import annotations
 
@@ -41,7 +43,7 @@ from typing import Iterable, Sequence
 import numpy as np
 
 # purposes of the independent streams
-_S_TEMP, _S_TARGET, _S_DRAFT, _S_TOKENS, _S_UNIF, _S_PEAKS = range(6)
+_S_TEMP, _S_TARGET, _S_DRAFT, _S_TOKENS, _S_UNIF, _S_PEAKS, _S_KROW = range(7)
 
 WORKLOADS = {
     # B=1, K=4, V=1000 float32; target ~ N(0, 2.0); draft = target + N(0, 0.5);
@@ -61,6 +63,9 @@ WORKLOADS = {
     # B=512, K=10, V=262144 bf16; target ~ N(0, 2.5) plus 1..4 peaks of +6;
     # draft = 0.8 target + N(0, 0.8); even rows T = 0.7, odd rows greedy.
     "large_vocab_stress": dict(id=5, B=512, K=10, V=262144, dtype="bf16"),
+    # adaptive verification: the Llama-3 rows (same generator), but row b
+    # verifies only its first K_b drafted tokens, K_b uniform in {0..4}.
+    "llama3_ragged": dict(id=6, gen=3, B=64, K=4, V=128256, dtype="bf16", ragged=True),
 }
 
 # the order of the five workloads, smallest first
@@ -86,6 +91,7 @@ class Workload:
     uniforms: np.ndarray       # [B, K+1] float32 in [0, 1)
     temperature: np.ndarray    # [B] float32, 0 = greedy row
     rows: np.ndarray           # [B] batch-row ids within the full workload
+    k_per_row: np.ndarray | None = None   # [B] int32 K_b (ragged workloads only)
 
     @property
     def elt(self) -> int:
@@ -125,7 +131,7 @@ def _zipf_row(rng: np.random.Generator, V: int) -> np.ndarray:
 def _temperature(name: str, seed: int, wid: int, b: int) -> float:
     if name in ("tiny_greedy", "greedy_batch"):
         return 0.0
-    if name in ("tiny_stochastic", "llama3_stochastic"):
+    if name in ("tiny_stochastic", "llama3_stochastic", "llama3_ragged"):
         return 1.0
     if name == "long_draft_mixed_t":
         if b % 10 == 0:
@@ -137,18 +143,19 @@ def _temperature(name: str, seed: int, wid: int, b: int) -> float:
 
 
 def _row(name: str, seed: int, b: int, K: int, V: int, dtype: str):
-    """Build batch row b: (target[K+1,V], draft[K,V], tokens[K], uniforms[K+1], T)."""
+    """Build batch row b: (target[K+1,V], draft[K,V], tokens[K], uniforms[K+1], T, K_b)."""
     wid = WORKLOADS[name]["id"]
+    gen = WORKLOADS[name].get("gen", wid)   # which value recipe (the id seeds the streams)
     T = _temperature(name, seed, wid, b)
     tgt64 = np.empty((K + 1, V))
     for t in range(K + 1):
         rng = _rng(seed, wid, b, _S_TARGET, t)
-        if wid == 1:
+        if gen == 1:
             row = rng.normal(0.0, 2.0, V)
-        elif wid == 2:
+        elif gen == 2:
             row = rng.normal(0.0, 3.0, V)
             row[_rng(seed, wid, b, _S_PEAKS, t).integers(0, V)] += 8.0
-        elif wid in (3, 4):
+        elif gen in (3, 4):
             row = _zipf_row(rng, V)
         else:
             row = rng.normal(0.0, 2.5, V)
@@ -159,13 +166,13 @@ def _row(name: str, seed: int, b: int, K: int, V: int, dtype: str):
     dr64 = np.empty((K, V))
     for t in range(K):
         rng = _rng(seed, wid, b, _S_DRAFT, t)
-        if wid == 1:
+        if gen == 1:
             dr64[t] = tgt64[t] + rng.normal(0.0, 0.5, V)
-        elif wid == 2:
+        elif gen == 2:
             dr64[t] = tgt64[t] + rng.normal(0.0, 1.0, V)
-        elif wid == 3:
+        elif gen == 3:
             dr64[t] = tgt64[t] + rng.normal(0.0, (0.2, 0.6, 1.2)[b % 3], V)
-        elif wid == 4:
+        elif gen == 4:
             dr64[t] = tgt64[t] + rng.normal(0.0, 0.5, V)
         else:
             dr64[t] = 0.8 * tgt64[t] + rng.normal(0.0, 0.8, V)
@@ -186,7 +193,8 @@ def _row(name: str, seed: int, b: int, K: int, V: int, dtype: str):
             tokens[t] = int(np.argmax(dstored[t] / np.float64(np.float32(T_draft)) + g))
     ints = _rng(seed, wid, b, _S_UNIF).integers(0, 1 << 24, K + 1)
     unif = (ints.astype(np.float64) * 2.0 ** -24).astype(np.float32)
-    return tgt, dr, tokens, unif, np.float32(T)
+    kb = int(_rng(seed, wid, b, _S_KROW).integers(0, K + 1)) if WORKLOADS[name].get("ragged") else K
+    return tgt, dr, tokens, unif, np.float32(T), kb
 
 
 def _rows_job(args):
@@ -212,6 +220,7 @@ def make(name: str, seed: int = 0, rows: Sequence[int] | None = None,
     tokens = np.empty((nb, K), np.int32)
     unif = np.empty((nb, K + 1), np.float32)
     temp = np.empty(nb, np.float32)
+    krow = np.empty(nb, np.int32)
     if workers is None:
         workers = 1
     main_file = getattr(sys.modules.get("__main__"), "__file__", None)
@@ -229,11 +238,11 @@ def make(name: str, seed: int = 0, rows: Sequence[int] | None = None,
         chunks = [rows]
     pos = {int(b): i for i, b in enumerate(rows)}
     for c, part in zip(chunks, parts):
-        for b, (tg, dr, tk, un, T) in zip(c, part):
+        for b, (tg, dr, tk, un, T, kb) in zip(c, part):
             i = pos[int(b)]
-            target[i], draft[i], tokens[i], unif[i], temp[i] = tg, dr, tk, un, T
+            target[i], draft[i], tokens[i], unif[i], temp[i], krow[i] = tg, dr, tk, un, T, kb
     return Workload(name, nb, K, V, dtype, target, draft, tokens, unif, temp,
-                    rows.astype(np.int64))
+                    rows.astype(np.int64), krow if cfg.get("ragged") else None)
 
 
 def default_workers() -> int:

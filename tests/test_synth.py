@@ -65,3 +65,17 @@ def test_drafted_tokens_follow_q_in_law():
         counts[np.argmax(d + -np.log(-np.log(U)))] += 1
     p = np.exp(d) / np.exp(d).sum()
     assert np.abs(counts / counts.sum() - p).max() < 0.03
+
+
+def test_ragged_workload_rows_and_lengths():
+    from speculative_decoding_verification_25_gb300 import synth
+    w = synth.make("llama3_ragged", seed=0, rows=[0, 5, 9])
+    assert w.k_per_row is not None and w.k_per_row.dtype == np.int32
+    assert ((w.k_per_row >= 0) & (w.k_per_row <= w.K)).all()
+    # the same rows rebuilt alone give the same lengths and values
+    w2 = synth.make("llama3_ragged", seed=0, rows=[9])
+    assert w2.k_per_row[0] == w.k_per_row[2]
+    np.testing.assert_array_equal(w2.target[0], w.target[2])
+    full = synth.make("llama3_ragged", seed=1, rows=range(64)).k_per_row
+    assert set(full.tolist()) == set(range(w.K + 1))   # every length occurs
+    assert synth.make("llama3_stochastic", seed=0, rows=[0]).k_per_row is None
