@@ -66,6 +66,7 @@ extern "C" {
 #define SV_DEV_BAD_TEMPERATURE 1u  /* T negative, NaN, infinite, or in (0, FLT_MIN) */
 #define SV_DEV_BAD_TOKEN 2u        /* a drafted token outside [0, V) */
 #define SV_DEV_NONFINITE 4u        /* a logit row without a finite maximum or sum */
+#define SV_DEV_BAD_K 8u            /* spec_verify_ragged: k_per_row[b] outside [0, K] */
 
 #define SV_MAX_K 16
 
@@ -114,6 +115,36 @@ int spec_verify(const void* target_logits, const void* draft_logits, int dtype,
                 int32_t* accepted_len, int32_t* out_tokens,
                 float* logp_out, float* logq_out,
                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Adaptive verification: row b verifies only its first K_b = k_per_row[b]
+ * drafted tokens (0 <= K_b <= K), as the stream transcript "IA local 202:
+ * acelere muito a geração com speculative decoding" (44:15-45:16, "adaptive
+ * verification") describes validating a different number of drafted
+ * tokens per request.
+ *
+ * The arrays keep spec_verify's padded [B, K+1] / [B, K] layouts with K the
+ * largest length.  Row b reads target rows 0..K_b, draft rows 0..K_b-1 (T > 0
+ * only), tokens x_0..x_{K_b-1}, acceptance draws r_0..r_{K_b-1} and its
+ * replacement/bonus draw u = uniforms[b, K_b]; nothing past its prefix is
+ * read.  It is spec_verify's rule on that prefix:
+ *   accepted_len[b]     0..K_b;
+ *   out_tokens[b, :]    accepted_len + 1 tokens, then -1 up to slot K;
+ *   logp_out / logq_out positions K_b..K-1 are NaN.
+ * K_b outside [0, K] makes an error row (accepted_len = -1, all tokens -1)
+ * and sets SV_DEV_BAD_K.
+ *
+ *   k_per_row   [B] int32, device, 4-byte aligned (NULL -> SV_ERR_NULL).
+ * Every other argument and the return codes are those of spec_verify; the
+ * workspace size is spec_verify_workspace_bytes(B, K, V, dtype).
+ */
+int spec_verify_ragged(const void* target_logits, const void* draft_logits, int dtype,
+                       const int32_t* draft_tokens, const float* uniforms,
+                       const float* temperature, const int32_t* k_per_row,
+                       int B, int K, int V,
+                       int32_t* accepted_len, int32_t* out_tokens,
+                       float* logp_out, float* logq_out,
+                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * The two stages spec_verify runs, for callers that schedule them apart

@@ -26,6 +26,7 @@ SV_ERR_TOO_LARGE = 7
 SV_DEV_BAD_TEMPERATURE = 1
 SV_DEV_BAD_TOKEN = 2
 SV_DEV_NONFINITE = 4
+SV_DEV_BAD_K = 8
 
 SV_MAX_K = 16
 SV_STATIC_SCRATCH_BYTES = 8 << 20
@@ -43,6 +44,8 @@ _SIG = {
                                        ctypes.c_size_t, _P]),
     "spec_verify_device_errors": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
     "spec_verify_static": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "spec_verify_ragged": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P,
+                                ctypes.c_size_t, _P]),
     "spec_verify_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -110,6 +113,16 @@ def spec_verify_accept_sample_raw(target_ptr, draft_ptr, dtype, tokens_ptr, unif
                                                 uniforms_ptr, temperature_ptr, B, K, V,
                                                 accepted_ptr, out_tokens_ptr, logp_ptr, logq_ptr,
                                                 workspace_ptr, workspace_bytes, stream_handle))
+
+
+def spec_verify_ragged_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr,
+                           temperature_ptr, k_per_row_ptr, B, K, V, accepted_ptr, out_tokens_ptr,
+                           logp_ptr, logq_ptr, workspace_ptr, workspace_bytes, stream_handle) -> int:
+    """spec_verify with a per-row number of verified drafts (k_per_row)."""
+    return int(load().spec_verify_ragged(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr,
+                                         temperature_ptr, k_per_row_ptr, B, K, V, accepted_ptr,
+                                         out_tokens_ptr, logp_ptr, logq_ptr, workspace_ptr,
+                                         workspace_bytes, stream_handle))
 
 
 def spec_verify_static_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr,

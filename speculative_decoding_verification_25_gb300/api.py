@@ -57,10 +57,15 @@ def workspace_for(B: int, K: int, V: int, dtype: int, device: torch.device) -> t
 
 def spec_verify(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor,
                 uniforms: torch.Tensor, temperature: torch.Tensor, *,
+                k_per_row: Optional[torch.Tensor] = None,
                 want_logprobs: bool = False, out: Optional[VerifyResult] = None,
                 workspace: Optional[torch.Tensor] = None,
                 stream: Optional[torch.cuda.Stream] = None) -> VerifyResult:
-    """Verify a batch on the current (or given) CUDA stream; no host sync."""
+    """Verify a batch on the current (or given) CUDA stream; no host sync.
+
+    ``k_per_row`` ([B] int32, optional): row b verifies only its first
+    k_per_row[b] drafted tokens (adaptive verification, spec_verify_ragged).
+    """
     if target.dim() != 3:
         raise ValueError("target must be [B, K+1, V]")
     B, K1, V = target.shape
@@ -83,12 +88,20 @@ def spec_verify(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.T
     if workspace is None:
         workspace = workspace_for(B, K, V, dt, dev)
     st = stream if stream is not None else torch.cuda.current_stream(dev)
-    status = N.spec_verify_raw(
-        target.data_ptr(), draft.data_ptr(), dt, draft_tokens.data_ptr(), uniforms.data_ptr(),
-        temperature.data_ptr(), B, K, V, out.accepted_len.data_ptr(), out.out_tokens.data_ptr(),
-        out.logp.data_ptr() if out.logp is not None else None,
-        out.logq.data_ptr() if out.logq is not None else None,
-        workspace.data_ptr(), workspace.numel() * workspace.element_size(), st.cuda_stream)
+    lp = out.logp.data_ptr() if out.logp is not None else None
+    lq = out.logq.data_ptr() if out.logq is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if k_per_row is None:
+        status = N.spec_verify_raw(
+            target.data_ptr(), draft.data_ptr(), dt, draft_tokens.data_ptr(), uniforms.data_ptr(),
+            temperature.data_ptr(), B, K, V, out.accepted_len.data_ptr(),
+            out.out_tokens.data_ptr(), lp, lq, workspace.data_ptr(), ws_bytes, st.cuda_stream)
+    else:
+        _check(k_per_row, "k_per_row", dtype=torch.int32, shape=(B,), device=dev)
+        status = N.spec_verify_ragged_raw(
+            target.data_ptr(), draft.data_ptr(), dt, draft_tokens.data_ptr(), uniforms.data_ptr(),
+            temperature.data_ptr(), k_per_row.data_ptr(), B, K, V, out.accepted_len.data_ptr(),
+            out.out_tokens.data_ptr(), lp, lq, workspace.data_ptr(), ws_bytes, st.cuda_stream)
     if status != N.SV_OK:
         raise N.SpecVerifyError(status)
     return out

@@ -164,8 +164,8 @@ bool vector_path(const void* target_logits, const void* draft_logits, int V, int
 }
 
 int launch_row_stats(const void* target_logits, const void* draft_logits, int dtype,
-                     const float* temperature, int B, int K, int V, void* workspace,
-                     DeviceCache* dc, cudaStream_t st) {
+                     const float* temperature, const int32_t* k_per_row, int B, int K, int V,
+                     void* workspace, DeviceCache* dc, cudaStream_t st) {
   const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
   const long long tpr = tiles_per_row(V, dtype);
   const long long n_target_rows = (long long)B * (K + 1);
@@ -179,6 +179,7 @@ int launch_row_stats(const void* target_logits, const void* draft_logits, int dt
   ra.tiles_per_row = (int)tpr;
   ra.n_tiles = (n_target_rows + (long long)B * K) * tpr;
   ra.n_target_rows = (int)n_target_rows;
+  ra.k_per_row = k_per_row;
   ra.partials = (float2*)((char*)workspace + partials_offset());
   ra.err = (unsigned*)workspace;
   // persistent grid: every SM filled once; every warp a contiguous tile range
@@ -197,9 +198,9 @@ int launch_row_stats(const void* target_logits, const void* draft_logits, int dt
 
 int launch_accept_sample(const void* target_logits, const void* draft_logits, int dtype,
                          const int32_t* draft_tokens, const float* uniforms,
-                         const float* temperature, int B, int K, int V, int32_t* accepted_len,
-                         int32_t* out_tokens, float* logp_out, float* logq_out, void* workspace,
-                         cudaStream_t st) {
+                         const float* temperature, const int32_t* k_per_row, int B, int K, int V,
+                         int32_t* accepted_len, int32_t* out_tokens, float* logp_out,
+                         float* logq_out, void* workspace, cudaStream_t st) {
   const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
   int cs, ngroups, gpc;
   cluster_geometry(V, dtype, &cs, &ngroups, &gpc);
@@ -217,6 +218,7 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
   aa.ngroups = ngroups;
   aa.groups_per_cta = gpc;
   aa.partials = (const float2*)((const char*)workspace + partials_offset());
+  aa.k_per_row = k_per_row;
   aa.err = (unsigned*)workspace;
   aa.accepted_len = accepted_len;
   aa.out_tokens = out_tokens;
@@ -239,6 +241,20 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelExC(&cfg, pick_accept(dtype, aligned), args);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// The whole step: the streaming launch, then the accept/sample launch.
+int launch_both(const void* target_logits, const void* draft_logits, int dtype,
+                const int32_t* draft_tokens, const float* uniforms, const float* temperature,
+                const int32_t* k_per_row, int B, int K, int V, int32_t* accepted_len,
+                int32_t* out_tokens, float* logp_out, float* logq_out, void* workspace,
+                DeviceCache* dc, cudaStream_t st) {
+  const int r = launch_row_stats(target_logits, draft_logits, dtype, temperature, k_per_row, B, K,
+                                 V, workspace, dc, st);
+  if (r != SV_OK) return r;
+  return launch_accept_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
+                              temperature, k_per_row, B, K, V, accepted_len, out_tokens, logp_out,
+                              logq_out, workspace, st);
 }
 
 DeviceCache* current_device_cache() {
@@ -298,8 +314,8 @@ int spec_verify_row_stats(const void* target_logits, const void* draft_logits, i
   if (st != SV_OK || B == 0) return st;
   DeviceCache* dc = current_device_cache();
   if (!dc) return SV_ERR_CUDA;
-  return launch_row_stats(target_logits, draft_logits, dtype, temperature, B, K, V, workspace, dc,
-                          (cudaStream_t)stream);
+  return launch_row_stats(target_logits, draft_logits, dtype, temperature, nullptr, B, K, V,
+                          workspace, dc, (cudaStream_t)stream);
 }
 
 int spec_verify_accept_sample(const void* target_logits, const void* draft_logits, int dtype,
@@ -314,8 +330,8 @@ int spec_verify_accept_sample(const void* target_logits, const void* draft_logit
   if (st != SV_OK || B == 0) return st;
   if (!current_device_cache()) return SV_ERR_CUDA;
   return launch_accept_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
-                              temperature, B, K, V, accepted_len, out_tokens, logp_out, logq_out,
-                              workspace, (cudaStream_t)stream);
+                              temperature, nullptr, B, K, V, accepted_len, out_tokens, logp_out,
+                              logq_out, workspace, (cudaStream_t)stream);
 }
 
 int spec_verify(const void* target_logits, const void* draft_logits, int dtype,
@@ -329,13 +345,27 @@ int spec_verify(const void* target_logits, const void* draft_logits, int dtype,
   if (st != SV_OK || B == 0) return st;
   DeviceCache* dc = current_device_cache();
   if (!dc) return SV_ERR_CUDA;
-  cudaStream_t s = (cudaStream_t)stream;
-  const int r = launch_row_stats(target_logits, draft_logits, dtype, temperature, B, K, V,
-                                 workspace, dc, s);
-  if (r != SV_OK) return r;
-  return launch_accept_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
-                              temperature, B, K, V, accepted_len, out_tokens, logp_out, logq_out,
-                              workspace, s);
+  return launch_both(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                     nullptr, B, K, V, accepted_len, out_tokens, logp_out, logq_out, workspace, dc,
+                     (cudaStream_t)stream);
+}
+
+int spec_verify_ragged(const void* target_logits, const void* draft_logits, int dtype,
+                       const int32_t* draft_tokens, const float* uniforms, const float* temperature,
+                       const int32_t* k_per_row, int B, int K, int V, int32_t* accepted_len,
+                       int32_t* out_tokens, float* logp_out, float* logq_out, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  const int st = validate(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                          B, K, V, accepted_len, out_tokens, logp_out, logq_out, workspace,
+                          workspace_bytes, true);
+  if (st != SV_OK || B == 0) return st;
+  if (!k_per_row) return SV_ERR_NULL;
+  if (!aligned_to(k_per_row, 4)) return SV_ERR_ALIGN;
+  DeviceCache* dc = current_device_cache();
+  if (!dc) return SV_ERR_CUDA;
+  return launch_both(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                     k_per_row, B, K, V, accepted_len, out_tokens, logp_out, logq_out, workspace,
+                     dc, (cudaStream_t)stream);
 }
 
 int spec_verify_static(const void* target_logits, const void* draft_logits, int dtype,
@@ -355,13 +385,9 @@ int spec_verify_static(const void* target_logits, const void* draft_logits, int 
                           B, K, V, accepted_len, out_tokens, logp_out, logq_out, scratch,
                           (size_t)SV_STATIC_SCRATCH_BYTES, true);
   if (st != SV_OK) return st;
-  cudaStream_t s = (cudaStream_t)stream;
-  const int r = launch_row_stats(target_logits, draft_logits, dtype, temperature, B, K, V,
-                                 scratch, dc, s);
-  if (r != SV_OK) return r;
-  return launch_accept_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
-                              temperature, B, K, V, accepted_len, out_tokens, logp_out, logq_out,
-                              scratch, s);
+  return launch_both(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                     nullptr, B, K, V, accepted_len, out_tokens, logp_out, logq_out, scratch, dc,
+                     (cudaStream_t)stream);
 }
 
 int spec_verify_device_errors(const void* workspace, void* stream, uint32_t* flags) {

@@ -38,6 +38,7 @@ constexpr float kBigProb = 1.0e-4f;
 constexpr unsigned kDevBadTemperature = 1u;
 constexpr unsigned kDevBadToken = 2u;
 constexpr unsigned kDevNonFinite = 4u;
+constexpr unsigned kDevBadK = 8u;
 
 // ============================================================== sampling group
 // The accept/sample code runs on a group of kP2Threads threads that starts
@@ -63,6 +64,7 @@ struct AcceptArgs {
   int ngroups;                // sampling groups per logit row
   int groups_per_cta;         // groups of one row owned by one CTA of the cluster
   const float2* partials;
+  const int32_t* k_per_row;   // [B] or nullptr (every row verifies K)
   unsigned* err;
   int32_t* accepted_len;
   int32_t* out_tokens;
@@ -101,6 +103,7 @@ struct AcceptSmem {
   float xq[kMaxK];
   int bad;
   int n;
+  int kb;   // drafted tokens this row verifies (K unless ragged)
   int redi[kP2Warps];
   CtaRecord rec;
   Decision dec;
@@ -603,18 +606,27 @@ __device__ void accept_inputs(const AcceptArgs& a, int b, float T, AcceptSmem& s
   const bool greedy = (T == 0.f);
   const long long ob = (long long)b * (K + 1);
   if ((gtid() >> 5) == 0) {
+    const int kb_in = a.k_per_row ? __ldg(a.k_per_row + b) : K;
+    const bool k_ok = kb_in >= 0 && kb_in <= K;
+    const int kb = k_ok ? kb_in : 0;
     int x = 0;
     bool tok_ok = true;
-    if (lane < K) {
+    if (lane < kb) {
       x = __ldg(a.tokens + (long long)b * K + lane);
       tok_ok = x >= 0 && x < a.V;
       sm.tok[lane] = x;
     }
-    if (lane <= K && !greedy) sm.r[lane] = __ldg(a.uniforms + ob + lane);
+    // r_0..r_{kb-1}, then u in column kb
+    if (lane <= kb && !greedy) sm.r[lane] = __ldg(a.uniforms + ob + lane);
     const bool all_ok = __all_sync(0xffffffffu, tok_ok);
-    if (lane == 0)
-      sm.bad = !valid_temperature(T) ? (int)kDevBadTemperature : (all_ok ? 0 : (int)kDevBadToken);
-    if (all_ok && !greedy && valid_temperature(T) && lane < K) {
+    if (lane == 0) {
+      sm.kb = kb;
+      sm.bad = !valid_temperature(T) ? (int)kDevBadTemperature
+               : !k_ok                ? (int)kDevBadK
+               : all_ok               ? 0
+                                      : (int)kDevBadToken;
+    }
+    if (all_ok && k_ok && !greedy && valid_temperature(T) && lane < kb) {
       sm.xp[lane] = E::load_scalar(a.target, (ob + lane) * (long long)a.V + x);
       sm.xq[lane] = E::load_scalar(a.draft, ((long long)b * K + lane) * (long long)a.V + x);
     }
@@ -708,14 +720,15 @@ __device__ __forceinline__ float2 fold_partials(const float2* pp, int tpr, bool 
 // argmax) for greedy rows.
 __device__ void fold_row_stats(const AcceptArgs& a, int b, bool greedy, AcceptSmem& sm) {
   constexpr int kHalves = kP2Threads / 16;
-  const int K = a.K, hl = gtid() & 15, hw = gtid() >> 4;
+  const int K = a.K, kb = sm.kb, hl = gtid() & 15, hw = gtid() >> 4;
   const long long tb = (long long)b * (K + 1);
   const long long db = a.n_target_rows + (long long)b * K;
   const int nrows = greedy ? K + 1 : 2 * K + 1;
   for (int base = 0; base < nrows; base += kHalves) {   // the same trip count in every warp
     const int rr = base + hw;
     const float2* pp = nullptr;
-    if (rr < nrows) {
+    // only the rows the row's K_b verifies: target 0..kb, draft 0..kb-1
+    if (rr < nrows && (rr <= K ? rr <= kb : rr - K - 1 < kb)) {
       const long long prow = (rr <= K) ? tb + rr : db + (rr - K - 1);
       pp = a.partials + prow * a.tiles_per_row;
     }
@@ -737,21 +750,23 @@ __device__ void accept_scan(const AcceptArgs& a, int b, float T, bool write, Acc
   const bool greedy = (T == 0.f);
   const long long ob = (long long)b * (K + 1);
   const int nrows = greedy ? K + 1 : 2 * K + 1;
+  const int kb = sm.kb;
   const float c = greedy ? 0.f : log2e_over_f(T);
   int bad = sm.bad;
   bool row_ok = true;
   for (int rr = lane; !bad && rr < nrows; rr += 32) {
+    if (rr <= K ? rr > kb : rr - K - 1 >= kb) continue;   // a row this K_b does not verify
     const float M = sm.rowMC[rr];
     row_ok = row_ok && isfinite(M) && (greedy || (isfinite(sm.rowS[rr]) && sm.rowS[rr] > 0.f));
   }
   if (!bad && !__all_sync(0xffffffffu, row_ok)) bad = (int)kDevNonFinite;
-  int n = K;
+  int n = kb;
   float lp = __int_as_float(0x7fffffff), lq = lp;
   if (!bad) {
     bool reject = false;
     if (greedy) {
-      reject = lane < K && sm.rowArg[lane] != sm.tok[lane];
-    } else if (lane < K) {
+      reject = lane < kb && sm.rowArg[lane] != sm.tok[lane];
+    } else if (lane < kb) {
       // log p_t(x_t) = (x c - MC) ln 2 - ln S, with x c - MC formed exactly by the FMA
       constexpr float kLn2 = 0.693147180559945309f;
       lp = __fmaf_rn(sm.xp[lane], c, -sm.rowMC[lane]) * kLn2 - logf(sm.rowS[lane]);
@@ -760,7 +775,7 @@ __device__ void accept_scan(const AcceptArgs& a, int b, float T, bool write, Acc
       reject = !(sm.r[lane] < expf(lp - lq));
     }
     const unsigned rej = __ballot_sync(0xffffffffu, reject);
-    n = rej ? __ffs(rej) - 1 : K;
+    n = rej ? __ffs(rej) - 1 : kb;
   }
   if (write) {
     if (lane < K) {
@@ -795,14 +810,14 @@ __device__ SampleCtx sample_ctx(const AcceptArgs& a, int b, float T, int g0, int
   const long long rowbytes = (long long)a.V * E::kBytes;
   SampleCtx x;
   x.rowP = (const char*)a.target + ((long long)b * (K + 1) + n) * rowbytes;
-  x.rowQ = (n < K) ? (const char*)a.draft + ((long long)b * K + n) * rowbytes : nullptr;
+  x.rowQ = (n < sm.kb) ? (const char*)a.draft + ((long long)b * K + n) * rowbytes : nullptr;
   x.V = a.V;
   x.g0 = g0;
   x.ng = ng;
   x.MCp = sm.rowMC[n];
-  x.MCq = (n < K) ? sm.rowMC[K + 1 + n] : 0.f;
+  x.MCq = (n < sm.kb) ? sm.rowMC[K + 1 + n] : 0.f;
   const float Sp32 = sm.rowS[n];
-  const float Sq32 = (n < K) ? sm.rowS[K + 1 + n] : 1.f;
+  const float Sq32 = (n < sm.kb) ? sm.rowS[K + 1 + n] : 1.f;
   x.L = log2e_over(T);
   // float32 path split of L with a strictly positive low part
   x.c_hi = x.L.hi;
@@ -845,8 +860,8 @@ __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptA
   // sampling at position n
   const int g0 = rank * a.groups_per_cta;
   SampleCtx x = sample_ctx<E>(a, b, T, g0, max(0, min(a.ngroups - g0, a.groups_per_cta)), sm);
-  const float u = sm.r[a.K];
-  bool residual = sm.n < a.K;
+  const float u = sm.r[sm.kb];
+  bool residual = sm.n < sm.kb;
   for (int attempt = 0; attempt < 2; ++attempt) {
     DF Wt, Qt;
     if (residual) sweep_slice<E, kAligned, true>(x, sm, s_part, Wt, Qt);

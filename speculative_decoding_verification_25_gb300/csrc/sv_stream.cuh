@@ -36,6 +36,7 @@ struct RowStatsArgs {
   int tiles_per_row;
   long long n_tiles;          // (B*(K+1) + B*K) * tiles_per_row
   int n_target_rows;          // B*(K+1)
+  const int32_t* k_per_row;   // [B] drafted tokens each row verifies, or nullptr (all K)
   float2* partials;           // [n_target_rows + B*K][tiles_per_row]
   unsigned* err;
 };
@@ -160,29 +161,41 @@ __device__ __forceinline__ void flush_stretch(float2* pp, int first, int last, b
 }
 
 // Everything a warp needs about the rows its range touches.  Lane i holds
-// the temperature of the range's i-th row; later rows (ranges over 32 rows
-// long, tiny vocabularies only) read theirs when they are reached.
+// the temperature (and verified length) of the range's i-th row's batch
+// row; later rows (ranges over 32 rows long, tiny vocabularies only) read
+// theirs when they are reached.
 struct WarpRows {
   const RowStatsArgs* a;
   long long t1;        // end of the range (stacked tile index)
   int row0;            // first row of the range
   float T_lane;
+  int kb_lane;
   unsigned act_mask;   // bit i: row row0 + i is read (i < 32)
 
   __device__ __forceinline__ int batch_of(int row) const {
     return row < a->n_target_rows ? row / (a->K + 1) : (row - a->n_target_rows) / a->K;
+  }
+  __device__ __forceinline__ int kb_of_batch(int b) const {
+    return a->k_per_row ? __ldg(a->k_per_row + b) : a->K;
   }
   __device__ __forceinline__ float T_of(int row) const {   // warp-uniform call
     const int d = row - row0;
     const float t = __shfl_sync(0xffffffffu, T_lane, d & 31);
     return d < 32 ? t : __ldg(a->temperature + batch_of(row));
   }
-  __device__ __forceinline__ bool row_read(int row, float T) const {
-    return valid_temperature(T) && !(row >= a->n_target_rows && T == 0.f);
+  // Is the row read?  Target rows 0..K_b and, for T > 0, draft rows
+  // 0..K_b-1 of a batch row with a valid temperature and 0 <= K_b <= K.
+  __device__ __forceinline__ bool row_read(int row, float T, int kb) const {
+    const bool draft = row >= a->n_target_rows;
+    const int b = batch_of(row);
+    const int pos = draft ? row - a->n_target_rows - b * a->K : row - b * (a->K + 1);
+    return valid_temperature(T) && !(draft && T == 0.f) && kb >= 0 && kb <= a->K &&
+           (draft ? pos < kb : pos <= kb);
   }
   __device__ __forceinline__ bool active(int row) const {   // warp-uniform call
     const int d = row - row0;
-    return d < 32 ? ((act_mask >> d) & 1u) != 0u : row_read(row, T_of(row));
+    if (d < 32) return ((act_mask >> d) & 1u) != 0u;
+    return row_read(row, T_of(row), kb_of_batch(batch_of(row)));
   }
   __device__ __forceinline__ const char* rowp(int row, int elem_bytes) const {
     const bool d = row >= a->n_target_rows;
@@ -283,8 +296,12 @@ __global__ void __launch_bounds__(kP1Threads, 4) sv_row_stats_kernel(RowStatsArg
   uint32_t wa[kTileVecsPerLane][4], wb[kTileVecsPerLane][4];
   load_at<E, kAligned>(wa, wr, pa, lane, full_end);
   const int row_last = (int)((t1 - 1) / tpr);
-  wr.T_lane = (wr.row0 + lane <= row_last) ? __ldg(a.temperature + wr.batch_of(wr.row0 + lane)) : 0.f;
-  wr.act_mask = __ballot_sync(0xffffffffu, wr.row0 + lane <= row_last && wr.row_read(wr.row0 + lane, wr.T_lane));
+  const bool lane_row = wr.row0 + lane <= row_last;
+  const int lane_b = lane_row ? wr.batch_of(wr.row0 + lane) : 0;
+  wr.T_lane = lane_row ? __ldg(a.temperature + lane_b) : 0.f;
+  wr.kb_lane = lane_row ? wr.kb_of_batch(lane_b) : 0;
+  wr.act_mask = __ballot_sync(0xffffffffu,
+                              lane_row && wr.row_read(wr.row0 + lane, wr.T_lane, wr.kb_lane));
 
   // one register ping-pong over the warp's active tiles, across row
   // boundaries: the next tile's loads are always in flight while the

@@ -42,10 +42,12 @@ class ParityReport:
 
 
 def _logprob_err(gpu, ref):
-    """Largest |difference|; equal infinities (a -inf logit) count as exact."""
+    """Largest |difference|; equal infinities (a -inf logit) count as exact,
+    and so do positions both sides mark NaN (positions a ragged row does not
+    verify); a NaN on one side only is an infinite error."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
-    same = (gpu == ref)
+    same = (gpu == ref) | (np.isnan(gpu) & np.isnan(ref))
     with np.errstate(invalid="ignore"):
         d = np.where(same, 0.0, np.abs(gpu - ref))
     d = np.where(np.isnan(d), np.inf, d)

@@ -25,10 +25,13 @@ def device_tensors(w, device="cuda:0", offset_elems=0):
             return t
         return host.to(device)
 
-    return dict(target=logits(w.target), draft=logits(w.draft),
-                draft_tokens=torch.from_numpy(w.draft_tokens).to(device),
-                uniforms=torch.from_numpy(w.uniforms).to(device),
-                temperature=torch.from_numpy(w.temperature).to(device))
+    d = dict(target=logits(w.target), draft=logits(w.draft),
+             draft_tokens=torch.from_numpy(w.draft_tokens).to(device),
+             uniforms=torch.from_numpy(w.uniforms).to(device),
+             temperature=torch.from_numpy(w.temperature).to(device))
+    if getattr(w, "k_per_row", None) is not None:
+        d["k_per_row"] = torch.from_numpy(np.ascontiguousarray(w.k_per_row, np.int32)).to(device)
+    return d
 
 
 def run_gpu(w, device="cuda:0", offset_elems=0, want_logprobs=True):
@@ -36,7 +39,8 @@ def run_gpu(w, device="cuda:0", offset_elems=0, want_logprobs=True):
     from speculative_decoding_verification_25_gb300 import api
     d = device_tensors(w, device, offset_elems)
     res = api.spec_verify(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
-                          d["temperature"], want_logprobs=want_logprobs)
+                          d["temperature"], k_per_row=d.get("k_per_row"),
+                          want_logprobs=want_logprobs)
     torch.cuda.synchronize()
     out = dict(accepted=res.accepted_len.cpu().numpy(), out_tokens=res.out_tokens.cpu().numpy(),
                logp=res.logp.cpu().numpy() if want_logprobs else None,
@@ -46,8 +50,10 @@ def run_gpu(w, device="cuda:0", offset_elems=0, want_logprobs=True):
 
 
 def _oracle_job(args):
-    target, draft, tokens, unif, temp, dtype = args
+    target, draft, tokens, unif, temp, dtype, kpr = args
     from oracle import oracle
+    if kpr is not None:
+        return oracle.spec_verify_ragged(target, draft, tokens, unif, temp, kpr, dtype=dtype)
     return oracle.spec_verify(target, draft, tokens, unif, temp, dtype=dtype)
 
 
@@ -57,8 +63,9 @@ def run_oracle(w, rows=None, workers=None):
     rows = np.arange(w.B) if rows is None else np.asarray(rows)
     workers = workers or max(1, min(16, os.cpu_count() or 1))
     chunks = [c for c in np.array_split(rows, min(workers, len(rows))) if len(c)]
-    jobs = [(w.target[c], w.draft[c], w.draft_tokens[c], w.uniforms[c], w.temperature[c], w.dtype)
-            for c in chunks]
+    kpr = getattr(w, "k_per_row", None)
+    jobs = [(w.target[c], w.draft[c], w.draft_tokens[c], w.uniforms[c], w.temperature[c], w.dtype,
+             None if kpr is None else kpr[c]) for c in chunks]
     if len(jobs) == 1:
         parts = [_oracle_job(jobs[0])]
     else:

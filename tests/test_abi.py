@@ -136,3 +136,14 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(ImportError):
         _native.load()
+
+
+def test_ragged_entry_point_checks_its_length_array(N):
+    def call(kpr, B=2):
+        return N.spec_verify_ragged_raw(FAKE, FAKE, N.SV_BF16, FAKE, FAKE, FAKE, kpr, B, 4, 1024,
+                                        FAKE, FAKE, None, None, FAKE, 1 << 30, None)
+    assert call(None) == N.SV_ERR_NULL
+    assert call(FAKE + 2) == N.SV_ERR_ALIGN
+    assert call(None, B=0) == N.SV_OK
+    assert N.spec_verify_ragged_raw(FAKE, FAKE, 9, FAKE, FAKE, FAKE, FAKE, 2, 4, 1024, FAKE, FAKE,
+                                    None, None, FAKE, 1 << 30, None) == N.SV_ERR_DTYPE
