@@ -81,16 +81,24 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def row_lengths(w):
+    """Drafted tokens each batch row verifies (K, or the ragged K_b)."""
+    kb = getattr(w, "k_per_row", None)
+    return np.full(w.B, w.K, np.int64) if kb is None else np.asarray(kb, np.int64)
+
+
 def algorithmic_bytes(w, accepted):
-    """Bytes the path must move for one batch: every target row, the draft rows
-    of rows with T > 0, and the re-read of the sampled position's rows
-    (2 rows on a rejection, 1 for a bonus; none for greedy rows)."""
+    """Bytes the path must move for one batch: the target rows 0..K_b of
+    every row, the draft rows 0..K_b-1 of rows with T > 0, and the re-read of
+    the sampled position's rows (2 rows on a rejection, 1 for a bonus; none
+    for greedy rows).  K_b = K unless the workload is ragged."""
     elt = w.elt
-    V, K = w.V, w.K
+    V = w.V
+    kb = row_lengths(w)
     stoch = w.temperature != 0
-    pass1 = w.B * (K + 1) * V * elt + int(stoch.sum()) * K * V * elt
-    rej = int(((accepted < K) & (accepted >= 0) & stoch).sum())
-    bonus = int(((accepted == K) & stoch).sum())
+    pass1 = int(((kb + 1) * V * elt).sum()) + int((kb * stoch).sum()) * V * elt
+    rej = int(((accepted < kb) & (accepted >= 0) & stoch).sum())
+    bonus = int(((accepted == kb) & stoch).sum())
     pass2 = (2 * rej + bonus) * V * elt
     return pass1, pass2
 
@@ -152,8 +160,11 @@ def _oracle_init(rows):
 
 def _oracle_job(idx):
     from oracle import oracle
-    target, draft, tokens, unif, temp, dtype = _ORACLE_ROWS
+    target, draft, tokens, unif, temp, dtype, kpr = _ORACLE_ROWS
     r = [idx % len(temp)]
+    if kpr is not None:
+        return oracle.spec_verify_ragged(target[r], draft[r], tokens[r], unif[r], temp[r],
+                                         kpr[r], dtype=dtype).accepted_len
     return oracle.spec_verify(target[r], draft[r], tokens[r], unif[r], temp[r],
                               dtype=dtype).accepted_len
 
@@ -164,8 +175,11 @@ def cpu_baseline(w, budget_s=12.0, sample_rows=4):
     over by a spawn pool (one worker per core) for about ``budget_s``."""
     import multiprocessing as mp
     cores = os.cpu_count() or 1
+    kpr = getattr(w, "k_per_row", None)
     rows = (w.target[:sample_rows], w.draft[:sample_rows], w.draft_tokens[:sample_rows],
-            w.uniforms[:sample_rows], w.temperature[:sample_rows], w.dtype)
+            w.uniforms[:sample_rows], w.temperature[:sample_rows], w.dtype,
+            None if kpr is None else kpr[:sample_rows])
+    pos_per_row = float((row_lengths(w)[:sample_rows] + 1).mean())
     ctx = mp.get_context("spawn")
     with ctx.Pool(cores, initializer=_oracle_init, initargs=(rows,)) as pool:
         pool.map(_oracle_job, range(cores))   # warm the workers (imports)
@@ -177,7 +191,7 @@ def cpu_baseline(w, budget_s=12.0, sample_rows=4):
                 break
         dt = time.perf_counter() - t0
         pool.terminate()
-    return {"value": done * (w.K + 1) / dt, "unit": "positions/s", "cores": cores,
+    return {"value": done * pos_per_row / dt, "unit": "positions/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{done} row verifications cycling over rows 0..{sample_rows - 1} of the "
                       f"{w.name} batch (K={w.K}, V={w.V}), float64 numpy, {cores} spawn "
@@ -193,10 +207,16 @@ def run_reference(args):
     w = synth.make(args.workload, seed=args.seed, rows=range(8))
     rows_per_step = 2
 
+    kb = row_lengths(w)
+
     def step(i):
         r = [(2 * i + k) % w.B for k in range(rows_per_step)]
-        oracle.spec_verify(w.target[r], w.draft[r], w.draft_tokens[r], w.uniforms[r],
-                           w.temperature[r], dtype=w.dtype)
+        if w.k_per_row is not None:
+            oracle.spec_verify_ragged(w.target[r], w.draft[r], w.draft_tokens[r], w.uniforms[r],
+                                      w.temperature[r], w.k_per_row[r], dtype=w.dtype)
+        else:
+            oracle.spec_verify(w.target[r], w.draft[r], w.draft_tokens[r], w.uniforms[r],
+                               w.temperature[r], dtype=w.dtype)
 
     for i in range(args.warmup):
         step(i)
@@ -204,7 +224,9 @@ def run_reference(args):
     for i in range(args.steps):
         step(i)
     dt = time.perf_counter() - t0
-    val = args.steps * rows_per_step * (w.K + 1) / dt
+    positions = sum(int(kb[(2 * i + k) % w.B]) + 1 for i in range(args.steps)
+                    for k in range(rows_per_step))
+    val = positions / dt
     cfg = synth.WORKLOADS[args.workload]
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "positions/s",
@@ -245,10 +267,13 @@ def run_ours(args):
         t = torch.from_numpy(a.view(np.int16) if w.dtype == "bf16" else a)
         return t.view(dt_torch) if w.dtype == "bf16" else t
 
+    ragged = w.k_per_row is not None
     host = dict(target=host_logits(w.target).pin_memory(), draft=host_logits(w.draft).pin_memory(),
                 draft_tokens=torch.from_numpy(w.draft_tokens).pin_memory(),
                 uniforms=torch.from_numpy(w.uniforms).pin_memory(),
                 temperature=torch.from_numpy(w.temperature).pin_memory())
+    if ragged:
+        host["k_per_row"] = torch.from_numpy(np.ascontiguousarray(w.k_per_row, np.int32)).pin_memory()
     copies = [{k: v.to(dev) for k, v in host.items()} for _ in range(args.copies)]
     ws_bytes = N.spec_verify_workspace_bytes(B, K, V, dtype_code)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -258,10 +283,17 @@ def run_ours(args):
     sh = stream.cuda_stream
 
     def call(c):
-        st = N.spec_verify_raw(c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
-                               c["draft_tokens"].data_ptr(), c["uniforms"].data_ptr(),
-                               c["temperature"].data_ptr(), B, K, V, acc.data_ptr(),
-                               outt.data_ptr(), None, None, ws.data_ptr(), ws_bytes, sh)
+        if ragged:
+            st = N.spec_verify_ragged_raw(c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
+                                          c["draft_tokens"].data_ptr(), c["uniforms"].data_ptr(),
+                                          c["temperature"].data_ptr(), c["k_per_row"].data_ptr(),
+                                          B, K, V, acc.data_ptr(), outt.data_ptr(), None, None,
+                                          ws.data_ptr(), ws_bytes, sh)
+        else:
+            st = N.spec_verify_raw(c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
+                                   c["draft_tokens"].data_ptr(), c["uniforms"].data_ptr(),
+                                   c["temperature"].data_ptr(), B, K, V, acc.data_ptr(),
+                                   outt.data_ptr(), None, None, ws.data_ptr(), ws_bytes, sh)
         if st != N.SV_OK:
             raise N.SpecVerifyError(st)
 
@@ -307,7 +339,9 @@ def run_ours(args):
     clocks = sampler.stop()
 
     # ---- per-kernel durations: the two stages with an event between them
-    n_split = max(args.steps, 50)
+    # (the stage entry points verify every row at K, so a ragged workload
+    # reports the step instead)
+    n_split = 0 if ragged else max(args.steps, 50)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in range(n_split)]
     barrier()
@@ -328,8 +362,8 @@ def run_ours(args):
     barrier()
     k1 = [a.elapsed_time(m) for a, m, _ in evs]
     k2 = [m.elapsed_time(e) for _, m, e in evs]
-    k1_ms = statistics.mean(k1)
-    k2_ms = statistics.mean(k2)
+    k1_ms = statistics.mean(k1) if k1 else None
+    k2_ms = statistics.mean(k2) if k2 else None
 
     # ---- end to end through the public call with host buffers
     d2h_acc = torch.empty(B, dtype=torch.int32).pin_memory()
@@ -341,7 +375,7 @@ def run_ours(args):
         for k in host:
             dst[k].copy_(host[k], non_blocking=True)
         r = api.spec_verify(dst["target"], dst["draft"], dst["draft_tokens"], dst["uniforms"],
-                            dst["temperature"], workspace=ws)
+                            dst["temperature"], k_per_row=dst.get("k_per_row"), workspace=ws)
         d2h_acc.copy_(r.accepted_len, non_blocking=True)
         d2h_tok.copy_(r.out_tokens, non_blocking=True)
 
@@ -365,13 +399,26 @@ def run_ours(args):
         return
 
     ms_per_step = t_ms / args.steps
-    positions = B * (K + 1) * world
+    # verified positions: K_b + 1 per row (the target positions the step checks)
+    positions = int((row_lengths(w) + 1).sum()) * world
     value = positions / (ms_per_step * 1e-3)
     p1_bytes, p2_bytes = algorithmic_bytes(w, accepted)
     hbm, peak_src = peaks()
-    k1_gbs = p1_bytes / (k1_ms * 1e-3) / 1e9
     step_gbs = (p1_bytes + p2_bytes) / (ms_per_step * 1e-3) / 1e9
-    traffic = stored_traffic(args.workload)
+    if k1_ms is not None:
+        # the streaming kernel, timed on its own
+        k1_gbs = p1_bytes / (k1_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": k1_gbs, "peak": hbm, "unit": "GB/s",
+                    "frac": k1_gbs / hbm, "traffic": stored_traffic(args.workload),
+                    "kernel": "sv_row_stats_kernel", "peak_source": peak_src,
+                    "bytes_per_launch": p1_bytes, "ms_per_launch": k1_ms}
+    else:
+        # both kernels as one step (ragged rows)
+        roofline = {"bound": "hbm", "achieved": step_gbs, "peak": hbm, "unit": "GB/s",
+                    "frac": step_gbs / hbm, "traffic": None,
+                    "kernel": "sv_row_stats_kernel + sv_accept_sample_kernel (one step)",
+                    "peak_source": peak_src, "bytes_per_launch": p1_bytes + p2_bytes,
+                    "ms_per_launch": ms_per_step}
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
@@ -382,14 +429,14 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": f"{args.workload} B={B} K={K} V={V} {w.dtype} logits",
-                   "B": B, "K": K, "V": V, "logits": w.dtype, "T": "1.0 all rows",
+                   "B": B, "K": K, "V": V, "logits": w.dtype,
+                   "T": describe_temperatures(w.temperature),
+                   "k_per_row": ("ragged: K_b uniform in 0..%d, mean %.2f" % (K, float(w.k_per_row.mean()))
+                                 if ragged else f"every row {K}"),
                    "l2": f"{len(copies)} rotating input copies of {w.logit_bytes() / 1e6:.2f} MB "
                          f"(each larger than the 129 MB L2)",
                    "parallelism": f"{world} independent replicas, own batch per GPU"},
-        "roofline": {"bound": "hbm", "achieved": k1_gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": k1_gbs / hbm, "traffic": traffic,
-                     "kernel": "sv_row_stats_kernel", "peak_source": peak_src,
-                     "bytes_per_launch": p1_bytes, "ms_per_launch": k1_ms},
+        "roofline": roofline,
         "step_roofline": {"achieved": step_gbs, "frac": step_gbs / hbm, "unit": "GB/s",
                           "bytes_per_step": p1_bytes + p2_bytes,
                           "accept_sample_ms_per_launch": k2_ms, "accept_sample_bytes": p2_bytes},
@@ -406,6 +453,17 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def describe_temperatures(T):
+    T = np.asarray(T)
+    greedy = int((T == 0).sum())
+    if greedy == len(T):
+        return "0 (greedy) all rows"
+    vals = np.unique(T[T != 0])
+    body = f"{vals[0]:g} all tempered rows" if len(vals) == 1 else \
+        f"{vals.min():.2f}..{vals.max():.2f} over tempered rows"
+    return body + (f", {greedy} greedy rows" if greedy else "")
 
 
 def stored_traffic(workload):

@@ -53,6 +53,31 @@ def test_algorithmic_bytes():
     assert p2 == (1 + 2) * V * 4                          # row 1 bonus (1 row), row 2 residual (2 rows)
 
 
+def test_algorithmic_bytes_ragged_rows():
+    sys.path.insert(0, ROOT)
+    import dataclasses
+    import bench
+    from speculative_decoding_verification_25_gb300 import synth
+    w = synth.make("llama3_ragged", seed=0, rows=[0, 1, 2])
+    w = dataclasses.replace(w, k_per_row=np.array([0, 2, 4], np.int32))
+    acc = np.array([0, 1, 4])                              # bonus, rejection at 1, bonus
+    p1, p2 = bench.algorithmic_bytes(w, acc)
+    V = w.V
+    # rows read: K_b + 1 target rows and K_b draft rows (all rows tempered)
+    assert p1 == ((0 + 1) + 0 + (2 + 1) + 2 + (4 + 1) + 4) * V * 2
+    assert p2 == (1 + 2 + 1) * V * 2
+    np.testing.assert_array_equal(bench.row_lengths(w), [0, 2, 4])
+
+
+def test_ragged_reference_arm_counts_verified_positions():
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "0", "--workload", "llama3_ragged"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert res.returncode == 0, res.stderr
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+
+
 def test_reference_arm_prints_one_json_line():
     res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                           "--steps", "1", "--warmup", "0", "--workload", "tiny_stochastic"],
