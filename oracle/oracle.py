@@ -67,6 +67,10 @@ R11 Logits may be -inf (probability 0); NaN and +inf are outside the
 R13 Adaptive verification (spec_verify_ragged): row b with K_b drafted
     tokens is the fixed-K rule on its prefix, with u = uniforms[b, K_b];
     K_b outside [0, K] makes an error row.
+R14 The plug step appends the n + 1 emitted tokens of a row at its current
+    length, drops what would land past the buffer (the row is then marked
+    clipped and its length stops at the buffer's end) and leaves error rows
+    unchanged.
 """
 from __future__ import annotations
 
@@ -315,6 +319,49 @@ def spec_verify_ragged(target_logits, draft_logits, draft_tokens, uniforms, temp
         rm[b, :kb], cm[b] = res.ratio_margin, res.cdf_margin
         modes.append(res.mode)
     return BatchResult(al, ot, lp, lq, rm, cm, modes)
+
+
+@dataclasses.dataclass
+class PlugResult:
+    tokens: np.ndarray       # [B, max_len] int32
+    seq_len: np.ndarray      # [B] int32
+    last_token: np.ndarray   # [B] int32 (unchanged where nothing was appended)
+    clipped: np.ndarray      # [B] bool: the row's tokens did not all fit
+
+
+def plug(accepted_len, out_tokens, tokens, seq_len, last_token=None) -> PlugResult:
+    """Write each row's emitted tokens into its sequence and advance its length,
+    on the device, so the next step needs no GPU-to-CPU read of the accepted
+    lengths ("Accelerating Sonar through speculation", the single-token MTP
+    schedule: once the target's input tokens are shifted, a kernel plugs the
+    next target tokens into their places; the accepted count otherwise forces
+    a GPU-to-CPU sync).
+
+    Reading R14: row b with accepted_len n >= 0 appends out_tokens[b, 0..n]
+    (n + 1 tokens) at tokens[b, L..L+n], L = seq_len[b], and sets seq_len[b]
+    to L + n + 1 and last_token[b] to out_tokens[b, n].  Tokens that would
+    land at or past max_len are dropped, seq_len stops at max_len and the row
+    is marked clipped.  An error row (n = -1) changes nothing.
+    """
+    tokens = np.array(tokens, np.int32, copy=True)
+    seq_len = np.array(seq_len, np.int32, copy=True)
+    B, max_len = tokens.shape
+    last = (np.full(B, -1, np.int32) if last_token is None
+            else np.array(last_token, np.int32, copy=True))
+    clipped = np.zeros(B, bool)
+    for b in range(B):
+        n = int(accepted_len[b])
+        if n < 0:
+            continue
+        L = int(seq_len[b])
+        for i in range(n + 1):
+            if L + i < max_len:
+                tokens[b, L + i] = out_tokens[b, i]
+            else:
+                clipped[b] = True
+        seq_len[b] = min(L + n + 1, max_len)
+        last[b] = out_tokens[b, n]
+    return PlugResult(tokens, seq_len, last, clipped)
 
 
 def expected_tokens_closed_form(alpha: float, K: int) -> float:
