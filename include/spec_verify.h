@@ -67,6 +67,8 @@ extern "C" {
 #define SV_DEV_BAD_TOKEN 2u        /* a drafted token outside [0, V) */
 #define SV_DEV_NONFINITE 4u        /* a logit row without a finite maximum or sum */
 #define SV_DEV_BAD_K 8u            /* spec_verify_ragged: k_per_row[b] outside [0, K] */
+#define SV_DEV_PLUG_CLIPPED 16u    /* spec_verify_plug: a row's tokens did not all fit */
+#define SV_DEV_BAD_LENGTH 32u      /* spec_verify_plug: seq_len[b] outside [0, max_len] */
 
 #define SV_MAX_K 16
 
@@ -225,6 +227,36 @@ int spec_verify_static(const void* target_logits, const void* draft_logits, int 
                        const float* temperature, int B, int K, int V,
                        int32_t* accepted_len, int32_t* out_tokens,
                        float* logp_out, float* logq_out, void* stream);
+
+/*
+ * The plug step: append each row's emitted tokens to its sequence buffer
+ * and advance its length on the device.  The next decode step can then be
+ * launched without reading the accepted lengths back to the host.  The page
+ * "Accelerating Sonar through speculation" (single-token MTP schedule) plugs
+ * the next target tokens into their places with a kernel, because the
+ * accepted count otherwise forces a GPU-to-CPU sync.
+ *
+ *   accepted_len [B]        int32, device: spec_verify's output (-1 = error row).
+ *   out_tokens   [B, K+1]   int32, device: spec_verify's output.
+ *   tokens       [B, max_len] int32, device, in/out: each row's sequence.
+ *   seq_len      [B]        int32, device, in/out: each row's current length.
+ *   last_token   [B]        int32, device, out, may be NULL: the last emitted
+ *                           token of each row (unchanged for rows not appended).
+ *   flags        one uint32, device, may be NULL: OR-ed with SV_DEV_PLUG_CLIPPED
+ *                or SV_DEV_BAD_LENGTH.
+ *
+ * For row b with n = accepted_len[b] >= 0 and L = seq_len[b] in
+ * [0, max_len], out_tokens[b, 0..n] goes to tokens[b, L..L+n] and seq_len[b]
+ * becomes L + n + 1.  Tokens that would land at or past max_len are dropped;
+ * seq_len then stops at max_len and SV_DEV_PLUG_CLIPPED is set.  Error rows
+ * are left unchanged; so are rows with L outside [0, max_len], which set
+ * SV_DEV_BAD_LENGTH.  Enqueue it on spec_verify's stream, after the call; it
+ * does not synchronise.  Returns SV_OK, SV_ERR_SHAPE (B < 0, K outside
+ * [1, SV_MAX_K], max_len < 1), SV_ERR_NULL, SV_ERR_ALIGN or SV_ERR_CUDA.
+ */
+int spec_verify_plug(const int32_t* accepted_len, const int32_t* out_tokens, int B, int K,
+                     int32_t* tokens, int32_t* seq_len, int max_len, int32_t* last_token,
+                     uint32_t* flags, void* stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* spec_verify_status_string(int status);

@@ -341,7 +341,8 @@ def plug(accepted_len, out_tokens, tokens, seq_len, last_token=None) -> PlugResu
     (n + 1 tokens) at tokens[b, L..L+n], L = seq_len[b], and sets seq_len[b]
     to L + n + 1 and last_token[b] to out_tokens[b, n].  Tokens that would
     land at or past max_len are dropped, seq_len stops at max_len and the row
-    is marked clipped.  An error row (n = -1) changes nothing.
+    is marked clipped.  An error row (n = -1), or a row whose length lies
+    outside [0, max_len], changes nothing.
     """
     tokens = np.array(tokens, np.int32, copy=True)
     seq_len = np.array(seq_len, np.int32, copy=True)
@@ -354,6 +355,8 @@ def plug(accepted_len, out_tokens, tokens, seq_len, last_token=None) -> PlugResu
         if n < 0:
             continue
         L = int(seq_len[b])
+        if L < 0 or L > max_len:
+            continue                           # a length outside the buffer: left unchanged
         for i in range(n + 1):
             if L + i < max_len:
                 tokens[b, L + i] = out_tokens[b, i]

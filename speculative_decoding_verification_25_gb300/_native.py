@@ -27,6 +27,8 @@ SV_DEV_BAD_TEMPERATURE = 1
 SV_DEV_BAD_TOKEN = 2
 SV_DEV_NONFINITE = 4
 SV_DEV_BAD_K = 8
+SV_DEV_PLUG_CLIPPED = 16
+SV_DEV_BAD_LENGTH = 32
 
 SV_MAX_K = 16
 SV_STATIC_SCRATCH_BYTES = 8 << 20
@@ -44,6 +46,7 @@ _SIG = {
                                        ctypes.c_size_t, _P]),
     "spec_verify_device_errors": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
     "spec_verify_static": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "spec_verify_plug": (_I, [_P, _P, _I, _I, _P, _P, _I, _P, _P, _P]),
     "spec_verify_ragged": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P,
                                 ctypes.c_size_t, _P]),
     "spec_verify_status_string": (ctypes.c_char_p, [_I]),
@@ -123,6 +126,13 @@ def spec_verify_ragged_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_pt
                                          temperature_ptr, k_per_row_ptr, B, K, V, accepted_ptr,
                                          out_tokens_ptr, logp_ptr, logq_ptr, workspace_ptr,
                                          workspace_bytes, stream_handle))
+
+
+def spec_verify_plug_raw(accepted_ptr, out_tokens_ptr, B, K, tokens_ptr, seq_len_ptr, max_len,
+                         last_token_ptr, flags_ptr, stream_handle) -> int:
+    """Append emitted tokens to the per-row sequences on the device."""
+    return int(load().spec_verify_plug(accepted_ptr, out_tokens_ptr, B, K, tokens_ptr, seq_len_ptr,
+                                       max_len, last_token_ptr, flags_ptr, stream_handle))
 
 
 def spec_verify_static_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr,

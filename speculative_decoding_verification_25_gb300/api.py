@@ -111,3 +111,30 @@ def device_errors(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] =
     """SV_DEV_* flags of the last call on ``workspace`` (synchronises the stream)."""
     st = stream if stream is not None else torch.cuda.current_stream(workspace.device)
     return N.spec_verify_device_errors(workspace.data_ptr(), st.cuda_stream)
+
+
+def plug(result: VerifyResult, tokens: torch.Tensor, seq_len: torch.Tensor, *,
+         last_token: Optional[torch.Tensor] = None, flags: Optional[torch.Tensor] = None,
+         stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Append each row's emitted tokens to ``tokens`` [B, max_len] (int32) at
+    ``seq_len`` [B] (int32, advanced in place) on the device; no host sync.
+    ``last_token`` [B] int32 receives each row's last emitted token;
+    ``flags`` (one int32) collects SV_DEV_PLUG_CLIPPED / SV_DEV_BAD_LENGTH."""
+    B, K1 = result.out_tokens.shape
+    dev = result.out_tokens.device
+    if tokens.dim() != 2 or tokens.shape[0] != B:
+        raise ValueError("tokens must be [B, max_len]")
+    _check(tokens, "tokens", dtype=torch.int32, device=dev)
+    _check(seq_len, "seq_len", dtype=torch.int32, shape=(B,), device=dev)
+    if last_token is not None:
+        _check(last_token, "last_token", dtype=torch.int32, shape=(B,), device=dev)
+    if flags is not None:
+        _check(flags, "flags", dtype=torch.int32, shape=(1,), device=dev)
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    status = N.spec_verify_plug_raw(
+        result.accepted_len.data_ptr(), result.out_tokens.data_ptr(), B, K1 - 1,
+        tokens.data_ptr(), seq_len.data_ptr(), tokens.shape[1],
+        last_token.data_ptr() if last_token is not None else None,
+        flags.data_ptr() if flags is not None else None, st.cuda_stream)
+    if status != N.SV_OK:
+        raise N.SpecVerifyError(status, "spec_verify_plug")

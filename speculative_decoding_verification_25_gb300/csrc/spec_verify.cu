@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "spec_verify.h"
+#include "sv_plug.cuh"
 #include "sv_sample.cuh"
 
 namespace {
@@ -388,6 +389,35 @@ int spec_verify_static(const void* target_logits, const void* draft_logits, int 
   return launch_both(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
                      nullptr, B, K, V, accepted_len, out_tokens, logp_out, logq_out, scratch, dc,
                      (cudaStream_t)stream);
+}
+
+int spec_verify_plug(const int32_t* accepted_len, const int32_t* out_tokens, int B, int K,
+                     int32_t* tokens, int32_t* seq_len, int max_len, int32_t* last_token,
+                     uint32_t* flags, void* stream) {
+  if (B < 0 || K < 1 || K > SV_MAX_K || max_len < 1) return SV_ERR_SHAPE;
+  if (B == 0) return SV_OK;
+  if (!accepted_len || !out_tokens || !tokens || !seq_len) return SV_ERR_NULL;
+  if (!aligned_to(accepted_len, 4) || !aligned_to(out_tokens, 4) || !aligned_to(tokens, 4) ||
+      !aligned_to(seq_len, 4) || (last_token && !aligned_to(last_token, 4)) ||
+      (flags && !aligned_to(flags, 4)))
+    return SV_ERR_ALIGN;
+  sv::PlugArgs pa;
+  pa.accepted_len = accepted_len;
+  pa.out_tokens = out_tokens;
+  pa.B = B;
+  pa.K = K;
+  pa.max_len = max_len;
+  pa.tokens = tokens;
+  pa.seq_len = seq_len;
+  pa.last_token = last_token;
+  pa.flags = flags;
+  const long long threads = (long long)B * 32;
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  void* args[] = {&pa};
+  return cudaLaunchKernel((void*)sv::sv_plug_kernel, dim3(blocks), dim3(256), args, 0,
+                          (cudaStream_t)stream) == cudaSuccess
+             ? SV_OK
+             : SV_ERR_CUDA;
 }
 
 int spec_verify_device_errors(const void* workspace, void* stream, uint32_t* flags) {

@@ -147,3 +147,16 @@ def test_ragged_entry_point_checks_its_length_array(N):
     assert call(None, B=0) == N.SV_OK
     assert N.spec_verify_ragged_raw(FAKE, FAKE, 9, FAKE, FAKE, FAKE, FAKE, 2, 4, 1024, FAKE, FAKE,
                                     None, None, FAKE, 1 << 30, None) == N.SV_ERR_DTYPE
+
+
+def test_plug_entry_point_checks_arguments(N):
+    def call(B=2, K=4, max_len=16, acc=FAKE, out=FAKE, tok=FAKE, L=FAKE, last=None, flags=None):
+        return N.spec_verify_plug_raw(acc, out, B, K, tok, L, max_len, last, flags, None)
+    assert call(B=0, acc=None, out=None, tok=None, L=None) == N.SV_OK
+    assert call(B=-1) == N.SV_ERR_SHAPE
+    assert call(K=0) == N.SV_ERR_SHAPE
+    assert call(max_len=0) == N.SV_ERR_SHAPE
+    for field in ("acc", "out", "tok", "L"):
+        assert call(**{field: None}) == N.SV_ERR_NULL, field
+    assert call(tok=FAKE + 2) == N.SV_ERR_ALIGN
+    assert call(flags=FAKE + 1) == N.SV_ERR_ALIGN

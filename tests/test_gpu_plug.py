@@ -1,0 +1,76 @@
+"""The plug step on the GPU against the oracle's plug (bit-exact)."""
+import numpy as np
+import pytest
+
+from speculative_decoding_verification_25_gb300 import synth
+
+from _parity import compare
+from gpu_util import device_tensors, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _states(rng, B, K, max_len):
+    acc = rng.integers(-1, K + 1, B).astype(np.int32)
+    out = np.full((B, K + 1), -1, np.int32)
+    for b in range(B):
+        if acc[b] >= 0:
+            out[b, :acc[b] + 1] = rng.integers(0, 50000, acc[b] + 1)
+    tok = rng.integers(0, 50000, (B, max_len)).astype(np.int32)
+    L = rng.integers(0, max_len + 1, B).astype(np.int32)
+    L[:3] = [max_len - 1, max_len, 0]
+    L[3:5] = [-1, max_len + 1]      # outside the buffer: left unchanged, flagged
+    return acc, out, tok, L
+
+
+def test_plug_matches_the_oracle_bit_for_bit():
+    import torch
+    from speculative_decoding_verification_25_gb300 import _native as N
+    from oracle import oracle
+    rng = np.random.default_rng(0)
+    B, K, max_len = 300, 5, 64
+    acc, out, tok, L = _states(rng, B, K, max_len)
+    dev = "cuda:0"
+    t_acc, t_out = torch.from_numpy(acc).to(dev), torch.from_numpy(out).to(dev)
+    t_tok, t_L = torch.from_numpy(tok).to(dev), torch.from_numpy(L).to(dev)
+    t_last = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    t_flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = N.spec_verify_plug_raw(t_acc.data_ptr(), t_out.data_ptr(), B, K, t_tok.data_ptr(),
+                                t_L.data_ptr(), max_len, t_last.data_ptr(), t_flags.data_ptr(),
+                                torch.cuda.current_stream().cuda_stream)
+    assert st == N.SV_OK
+    torch.cuda.synchronize()
+    ref = oracle.plug(acc, out, tok, L, last_token=np.full(B, -7, np.int32))
+    np.testing.assert_array_equal(t_tok.cpu().numpy(), ref.tokens)
+    np.testing.assert_array_equal(t_L.cpu().numpy(), ref.seq_len)
+    np.testing.assert_array_equal(t_last.cpu().numpy(), ref.last_token)
+    flags = int(t_flags.item())
+    assert bool(flags & N.SV_DEV_PLUG_CLIPPED) == bool(ref.clipped.any())
+    assert flags & N.SV_DEV_BAD_LENGTH
+
+
+def test_verify_then_plug_on_the_device():
+    import torch
+    from speculative_decoding_verification_25_gb300 import api
+    from oracle import oracle
+    w = synth.make("llama3_stochastic", seed=4, rows=range(24))
+    d = device_tensors(w)
+    rng = np.random.default_rng(1)
+    max_len = 40
+    tok = rng.integers(0, w.V, (w.B, max_len)).astype(np.int32)
+    L = rng.integers(0, max_len - w.K, w.B).astype(np.int32)
+    t_tok = torch.from_numpy(tok).to("cuda:0")
+    t_L = torch.from_numpy(L).to("cuda:0")
+    last = torch.empty(w.B, dtype=torch.int32, device="cuda:0")
+    r = api.spec_verify(d["target"], d["draft"], d["draft_tokens"], d["uniforms"], d["temperature"],
+                        want_logprobs=True)
+    api.plug(r, t_tok, t_L, last_token=last)          # same stream, no host read in between
+    torch.cuda.synchronize()
+    ref = run_oracle(w, workers=1)
+    rep = compare(ref, r.accepted_len.cpu().numpy(), r.out_tokens.cpu().numpy(),
+                  r.logp.cpu().numpy(), r.logq.cpu().numpy(), w.temperature)
+    assert not rep.failures and rep.mismatched_rows == 0
+    want = oracle.plug(ref.accepted_len, ref.out_tokens, tok, L)
+    np.testing.assert_array_equal(t_tok.cpu().numpy(), want.tokens)
+    np.testing.assert_array_equal(t_L.cpu().numpy(), want.seq_len)
+    np.testing.assert_array_equal(last.cpu().numpy(), want.last_token)

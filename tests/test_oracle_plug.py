@@ -45,3 +45,12 @@ def test_invariants_on_random_states():
         assert (r.tokens[b, l0 + fit:] == tok[b, l0 + fit:]).all()
         assert r.clipped[b] == (fit < n + 1)
         assert r.last_token[b] == out[b, n]
+
+
+def test_length_outside_the_buffer_leaves_the_row():
+    acc = np.array([1, 1])
+    out = np.array([[5, 6], [7, 8]])
+    tok = np.zeros((2, 4), np.int32)
+    r = oracle.plug(acc, out, tok, np.array([-1, 5]))
+    np.testing.assert_array_equal(r.seq_len, [-1, 5])
+    assert (r.tokens == 0).all() and not r.clipped.any()
