@@ -67,6 +67,10 @@ R11 Logits may be -inf (probability 0); NaN and +inf are outside the
 R13 Adaptive verification (spec_verify_ragged): row b with K_b drafted
     tokens is the fixed-K rule on its prefix, with u = uniforms[b, K_b];
     K_b outside [0, K] makes an error row.
+R15 Greedy tree verification: a node is accepted iff its parent is (or is
+    the root) and its token is the target argmax at the parent's slot; the
+    deepest accepted node (lowest index on ties) gives the path, plus the
+    argmax at its own slot.
 R14 The plug step appends the n + 1 emitted tokens of a row at its current
     length, drops what would land past the buffer (the row is then marked
     clipped and its length stops at the buffer's end) and leaves error rows
@@ -319,6 +323,84 @@ def spec_verify_ragged(target_logits, draft_logits, draft_tokens, uniforms, temp
         rm[b, :kb], cm[b] = res.ratio_margin, res.cdf_margin
         modes.append(res.mode)
     return BatchResult(al, ot, lp, lq, rm, cm, modes)
+
+
+@dataclasses.dataclass
+class TreeResult:
+    accepted_len: np.ndarray    # [B] int32: depth of the accepted path (-1 = error row)
+    out_tokens: np.ndarray      # [B, N+1] int32: path tokens, then the bonus token, then -1
+    accepted_nodes: np.ndarray  # [B, N] int32: node indices along the path, then -1
+
+
+def verify_tree_greedy_row(target: np.ndarray, node_tokens: np.ndarray,
+                           parents: np.ndarray):
+    """Greedy verification of one draft tree.
+
+    The lesson's section "Verificação de Atenção em Árvore" checks every node
+    of a draft tree in one target pass, keeping the longest prefix along any
+    accepted path; its exercise 4 asks that the target accept the longest
+    correct branch.  The Sonar page's EAGLE section keeps the longest
+    acceptable sequence and adds one token from the target.
+
+    Reading R15: node i has token node_tokens[i] and parent parents[i]
+    (-1 = the root, else an earlier node, so parents[i] < i).  target[0] is
+    the slot after the context (the root) and target[i + 1] the slot after
+    node i.  Node i is accepted iff its parent is the root or accepted, and
+    node_tokens[i] == argmax(target[slot of its parent]) (np.argmax, lowest
+    index on ties).  The deepest accepted node wins, with ties going to the
+    lowest node index.  The output is the tokens along its path, then the
+    bonus argmax(target[its slot]).  With no node accepted, the output is
+    the root's argmax alone.  A parent outside [-1, i) or a token outside
+    [0, V) makes an error row.
+    Returns (depth, tokens along the path + bonus, nodes along the path).
+    """
+    target = np.asarray(target, np.float64)
+    N = len(node_tokens)
+    V = target.shape[1]
+    for i in range(N):
+        if not (-1 <= int(parents[i]) < i) or not (0 <= int(node_tokens[i]) < V):
+            return -1, [], []
+    if not np.isfinite(target.max(axis=1)).all():
+        return -1, [], []
+    am = [int(np.argmax(target[s])) for s in range(N + 1)]
+    accepted = np.zeros(N, bool)
+    depth = np.zeros(N, np.int64)
+    for i in range(N):                       # parents come first
+        p = int(parents[i])
+        ok_parent = p < 0 or accepted[p]
+        slot = 0 if p < 0 else p + 1
+        accepted[i] = ok_parent and int(node_tokens[i]) == am[slot]
+        depth[i] = 1 if p < 0 else depth[p] + 1
+    best = -1
+    for i in range(N):
+        if accepted[i] and (best < 0 or depth[i] > depth[best]):
+            best = i
+    if best < 0:
+        return 0, [am[0]], []
+    path = []
+    i = best
+    while i >= 0:
+        path.append(i)
+        i = int(parents[i])
+    path.reverse()
+    return len(path), [int(node_tokens[i]) for i in path] + [am[best + 1]], path
+
+
+def verify_tree_greedy(target_logits, node_tokens, parents, dtype: str | None = None) -> TreeResult:
+    """The whole batch: target_logits [B, N+1, V], node_tokens and parents [B, N]."""
+    B, N = np.asarray(node_tokens).shape
+    al = np.empty(B, np.int32)
+    ot = np.full((B, N + 1), -1, np.int32)
+    nodes = np.full((B, N), -1, np.int32)
+    for b in range(B):
+        tg = target_logits[b]
+        if dtype is not None:
+            tg = decode_logits(tg, dtype)
+        d, toks, path = verify_tree_greedy_row(tg, np.asarray(node_tokens[b]), np.asarray(parents[b]))
+        al[b] = d
+        ot[b, :len(toks)] = toks
+        nodes[b, :len(path)] = path
+    return TreeResult(al, ot, nodes)
 
 
 @dataclasses.dataclass

@@ -32,6 +32,11 @@ without generating the rest):
   column K is the single draw u used for the replacement or bonus token.
 * the ragged workload also draws, per batch row, how many drafted tokens
   the row verifies: K_b uniform in {0, ..., K} (its draw u is column K_b).
+* the tree workload drafts a fixed tree per row (branching 3, 2, 1, 1 by
+  depth: 21 nodes, parents listed before children); its target slots are
+  N(0, 2) logits (slot 0 after the context, slot i + 1 after node i).  The
+  first child of every slot takes that slot's argmax with probability 0.75,
+  and every other node takes a uniform token.
 """
 from __future__ import annotations
 
@@ -43,7 +48,7 @@ from typing import Iterable, Sequence
 import numpy as np
 
 # purposes of the independent streams
-_S_TEMP, _S_TARGET, _S_DRAFT, _S_TOKENS, _S_UNIF, _S_PEAKS, _S_KROW = range(7)
+_S_TEMP, _S_TARGET, _S_DRAFT, _S_TOKENS, _S_UNIF, _S_PEAKS, _S_KROW, _S_TREE = range(8)
 
 WORKLOADS = {
     # B=1, K=4, V=1000 float32; target ~ N(0, 2.0); draft = target + N(0, 0.5);
@@ -66,6 +71,9 @@ WORKLOADS = {
     # adaptive verification: the Llama-3 rows (same generator), but row b
     # verifies only its first K_b drafted tokens, K_b uniform in {0..4}.
     "llama3_ragged": dict(id=6, gen=3, B=64, K=4, V=128256, dtype="bf16", ragged=True),
+    # greedy tree verification at the Llama-3 vocabulary: B=64 rows, a
+    # 21-node draft tree each (K = N = 21 nodes, N + 1 target slots), bf16.
+    "llama3_tree": dict(id=7, B=64, K=21, V=128256, dtype="bf16", tree=(3, 2, 1, 1)),
 }
 
 # the order of the five workloads, smallest first
@@ -92,6 +100,7 @@ class Workload:
     temperature: np.ndarray    # [B] float32, 0 = greedy row
     rows: np.ndarray           # [B] batch-row ids within the full workload
     k_per_row: np.ndarray | None = None   # [B] int32 K_b (ragged workloads only)
+    parents: np.ndarray | None = None     # [B, N] int32 tree parents (tree workloads only)
 
     @property
     def elt(self) -> int:
@@ -197,8 +206,48 @@ def _row(name: str, seed: int, b: int, K: int, V: int, dtype: str):
     return tgt, dr, tokens, unif, np.float32(T), kb
 
 
+def tree_parents(branching) -> np.ndarray:
+    """Parents of a fixed tree, breadth first: every node of depth d has
+    branching[d] children; -1 is the root."""
+    parents = []
+    level = [-1]
+    for width in branching:
+        nxt = []
+        for p in level:
+            for _ in range(width):
+                parents.append(p)
+                nxt.append(len(parents) - 1)
+        level = nxt
+    return np.asarray(parents, np.int32)
+
+
+def _tree_row(name: str, seed: int, b: int, N: int, V: int, dtype: str):
+    """Batch row b of a tree workload: (target[N+1,V], node tokens[N], parents[N])."""
+    wid = WORKLOADS[name]["id"]
+    parents = tree_parents(WORKLOADS[name]["tree"])
+    assert len(parents) == N
+    tgt64 = np.empty((N + 1, V))
+    for s in range(N + 1):
+        tgt64[s] = _rng(seed, wid, b, _S_TARGET, s).normal(0.0, 2.0, V)
+    tgt = _store(tgt64, dtype)
+    am = _stored_as_f64(tgt, dtype).argmax(axis=1)   # lowest index on ties
+    pick = _rng(seed, wid, b, _S_TREE)
+    tokens = np.empty(N, np.int32)
+    first_child = {}
+    for i in range(N):
+        slot = 0 if parents[i] < 0 else int(parents[i]) + 1
+        first = slot not in first_child
+        first_child.setdefault(slot, i)
+        match = pick.random() < 0.75
+        rnd = int(pick.integers(0, V))
+        tokens[i] = int(am[slot]) if (first and match) else rnd
+    return tgt, tokens, parents
+
+
 def _rows_job(args):
     name, seed, rows, K, V, dtype = args
+    if WORKLOADS[name].get("tree"):
+        return [_tree_row(name, seed, b, K, V, dtype) for b in rows]
     return [_row(name, seed, b, K, V, dtype) for b in rows]
 
 
@@ -216,7 +265,7 @@ def make(name: str, seed: int = 0, rows: Sequence[int] | None = None,
     nb = len(rows)
     sdt = np.float32 if dtype == "f32" else np.uint16
     target = np.empty((nb, K + 1, V), sdt)
-    draft = np.empty((nb, K, V), sdt)
+    draft = np.empty((nb, 0 if cfg.get("tree") else K, V), sdt)
     tokens = np.empty((nb, K), np.int32)
     unif = np.empty((nb, K + 1), np.float32)
     temp = np.empty(nb, np.float32)
@@ -237,6 +286,16 @@ def make(name: str, seed: int = 0, rows: Sequence[int] | None = None,
         parts = [_rows_job((name, seed, [int(b) for b in rows], K, V, dtype))]
         chunks = [rows]
     pos = {int(b): i for i, b in enumerate(rows)}
+    if cfg.get("tree"):
+        par = np.empty((nb, K), np.int32)
+        for c, part in zip(chunks, parts):
+            for b, (tg, tk, pa) in zip(c, part):
+                i = pos[int(b)]
+                target[i], tokens[i], par[i] = tg, tk, pa
+        # no draft rows, uniforms or temperatures: greedy verification of the tree
+        return Workload(name, nb, K, V, dtype, target, np.empty((nb, 0, V), sdt), tokens,
+                        np.zeros((nb, K + 1), np.float32), np.zeros(nb, np.float32),
+                        rows.astype(np.int64), None, par)
     for c, part in zip(chunks, parts):
         for b, (tg, dr, tk, un, T, kb) in zip(c, part):
             i = pos[int(b)]

@@ -79,3 +79,16 @@ def test_ragged_workload_rows_and_lengths():
     full = synth.make("llama3_ragged", seed=1, rows=range(64)).k_per_row
     assert set(full.tolist()) == set(range(w.K + 1))   # every length occurs
     assert synth.make("llama3_stochastic", seed=0, rows=[0]).k_per_row is None
+
+
+def test_tree_workload_shape_and_parents():
+    from speculative_decoding_verification_25_gb300 import synth
+    np.testing.assert_array_equal(synth.tree_parents((2, 1)), [-1, -1, 0, 1])
+    w = synth.make("llama3_tree", seed=0, rows=[0, 3])
+    N = w.K
+    assert w.parents.shape == (2, N) and w.target.shape == (2, N + 1, w.V)
+    assert all(-1 <= w.parents[0, i] < i for i in range(N))
+    assert ((w.draft_tokens >= 0) & (w.draft_tokens < w.V)).all()
+    assert (w.temperature == 0).all()
+    w2 = synth.make("llama3_tree", seed=0, rows=[3])
+    np.testing.assert_array_equal(w2.draft_tokens[0], w.draft_tokens[1])
