@@ -69,8 +69,10 @@ extern "C" {
 #define SV_DEV_BAD_K 8u            /* spec_verify_ragged: k_per_row[b] outside [0, K] */
 #define SV_DEV_PLUG_CLIPPED 16u    /* spec_verify_plug: a row's tokens did not all fit */
 #define SV_DEV_BAD_LENGTH 32u      /* spec_verify_plug: seq_len[b] outside [0, max_len] */
+#define SV_DEV_BAD_TREE 64u        /* spec_verify_tree: a parent or node token out of range */
 
 #define SV_MAX_K 16
+#define SV_MAX_TREE_NODES 128
 
 /*
  * Bytes of scratch the caller must pass to spec_verify for this shape.
@@ -227,6 +229,41 @@ int spec_verify_static(const void* target_logits, const void* draft_logits, int 
                        const float* temperature, int B, int K, int V,
                        int32_t* accepted_len, int32_t* out_tokens,
                        float* logp_out, float* logq_out, void* stream);
+
+/*
+ * Greedy verification of a draft tree per row.  The lesson's section
+ * "Verificação de Atenção em Árvore" checks every node of the tree in one
+ * target pass and keeps the longest prefix along an accepted path.  Its
+ * exercise 4 asks that the target accept the longest correct branch.
+ *
+ *   target_logits  [B, N+1, V] of dtype: slot 0 follows the context (the
+ *                  root), slot i+1 follows node i.
+ *   node_tokens    [B, N] int32: the token of every node.
+ *   parents        [B, N] int32: -1 (a child of the root) or an earlier node
+ *                  (parents[b, i] < i; breadth-first order satisfies this).
+ *   accepted_len   [B] int32 out: depth of the accepted path, 0..N (-1 = error row).
+ *   out_tokens     [B, N+1] int32 out: the tokens along the path, then the
+ *                  target's argmax at its last node's slot (the root's slot
+ *                  if no node is accepted), then -1.
+ *   accepted_nodes [B, N] int32 out, may be NULL: the node indices along the
+ *                  path, then -1.
+ *   workspace      at least spec_verify_tree_workspace_bytes(B, N, V, dtype)
+ *                  bytes, 16-byte aligned; needs no initialisation.
+ *
+ * Node i is accepted iff its parent is the root or accepted, and its token
+ * equals argmax(target slot of the parent) (lowest index on ties).  The
+ * deepest accepted node wins, with the lowest node index on ties.  A parent
+ * outside [-1, i), a node token outside [0, V) or a slot with no finite
+ * maximum makes an error row and sets SV_DEV_BAD_TREE / SV_DEV_NONFINITE
+ * (read with spec_verify_device_errors).  1 <= N <= SV_MAX_TREE_NODES.
+ * Returns the status codes of spec_verify.
+ */
+size_t spec_verify_tree_workspace_bytes(int B, int N, int V, int dtype);
+
+int spec_verify_tree(const void* target_logits, int dtype, const int32_t* node_tokens,
+                     const int32_t* parents, int B, int N, int V, int32_t* accepted_len,
+                     int32_t* out_tokens, int32_t* accepted_nodes, void* workspace,
+                     size_t workspace_bytes, void* stream);
 
 /*
  * The plug step: append each row's emitted tokens to its sequence buffer

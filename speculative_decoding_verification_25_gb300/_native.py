@@ -29,8 +29,10 @@ SV_DEV_NONFINITE = 4
 SV_DEV_BAD_K = 8
 SV_DEV_PLUG_CLIPPED = 16
 SV_DEV_BAD_LENGTH = 32
+SV_DEV_BAD_TREE = 64
 
 SV_MAX_K = 16
+SV_MAX_TREE_NODES = 128
 SV_STATIC_SCRATCH_BYTES = 8 << 20
 
 # every function of include/spec_verify.h: (restype, argtypes)
@@ -46,6 +48,8 @@ _SIG = {
                                        ctypes.c_size_t, _P]),
     "spec_verify_device_errors": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
     "spec_verify_static": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "spec_verify_tree_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "spec_verify_tree": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "spec_verify_plug": (_I, [_P, _P, _I, _I, _P, _P, _I, _P, _P, _P]),
     "spec_verify_ragged": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P,
                                 ctypes.c_size_t, _P]),
@@ -126,6 +130,19 @@ def spec_verify_ragged_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_pt
                                          temperature_ptr, k_per_row_ptr, B, K, V, accepted_ptr,
                                          out_tokens_ptr, logp_ptr, logq_ptr, workspace_ptr,
                                          workspace_bytes, stream_handle))
+
+
+def spec_verify_tree_workspace_bytes(B: int, N: int, V: int, dtype: int) -> int:
+    return int(load().spec_verify_tree_workspace_bytes(B, N, V, dtype))
+
+
+def spec_verify_tree_raw(target_ptr, dtype, node_tokens_ptr, parents_ptr, B, N, V, accepted_ptr,
+                         out_tokens_ptr, accepted_nodes_ptr, workspace_ptr, workspace_bytes,
+                         stream_handle) -> int:
+    """Greedy verification of one draft tree per row."""
+    return int(load().spec_verify_tree(target_ptr, dtype, node_tokens_ptr, parents_ptr, B, N, V,
+                                       accepted_ptr, out_tokens_ptr, accepted_nodes_ptr,
+                                       workspace_ptr, workspace_bytes, stream_handle))
 
 
 def spec_verify_plug_raw(accepted_ptr, out_tokens_ptr, B, K, tokens_ptr, seq_len_ptr, max_len,

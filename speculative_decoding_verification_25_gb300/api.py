@@ -15,6 +15,7 @@ from typing import NamedTuple, Optional
 import torch
 
 from . import _native as N
+from . import _native as _N
 
 _DTYPES = {torch.bfloat16: N.SV_BF16, torch.float32: N.SV_F32}
 _workspaces: dict = {}
@@ -138,3 +139,45 @@ def plug(result: VerifyResult, tokens: torch.Tensor, seq_len: torch.Tensor, *,
         flags.data_ptr() if flags is not None else None, st.cuda_stream)
     if status != N.SV_OK:
         raise N.SpecVerifyError(status, "spec_verify_plug")
+
+
+class TreeResult(NamedTuple):
+    accepted_len: torch.Tensor                  # [B] int32: depth of the accepted path, -1 = error row
+    out_tokens: torch.Tensor                    # [B, N+1] int32: path tokens, bonus, -1 padded
+    accepted_nodes: Optional[torch.Tensor] = None   # [B, N] int32: path node indices, -1 padded
+
+
+def verify_tree(target: torch.Tensor, node_tokens: torch.Tensor, parents: torch.Tensor, *,
+                want_nodes: bool = False, workspace: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> TreeResult:
+    """Greedy verification of one draft tree per row (spec_verify_tree):
+    ``target`` [B, N+1, V] (slot 0 after the context, slot i+1 after node i),
+    ``node_tokens`` and ``parents`` [B, N] int32 (parents[b, i] in [-1, i))."""
+    if target.dim() != 3:
+        raise ValueError("target must be [B, N+1, V]")
+    B, N1, V = target.shape
+    N = N1 - 1
+    dev = target.device
+    if target.dtype not in _DTYPES:
+        raise TypeError(f"target dtype {target.dtype} is not bfloat16 or float32")
+    dt = _DTYPES[target.dtype]
+    _check(target, "target", device=dev)
+    _check(node_tokens, "node_tokens", dtype=torch.int32, shape=(B, N), device=dev)
+    _check(parents, "parents", dtype=torch.int32, shape=(B, N), device=dev)
+    need = _N.spec_verify_tree_workspace_bytes(B, N, V, dt)
+    if need == 0:
+        raise ValueError(f"invalid tree shape B={B} N={N} V={V}")
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    res = TreeResult(torch.empty(B, dtype=torch.int32, device=dev),
+                     torch.empty(B, N + 1, dtype=torch.int32, device=dev),
+                     torch.empty(B, N, dtype=torch.int32, device=dev) if want_nodes else None)
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    status = _N.spec_verify_tree_raw(
+        target.data_ptr(), dt, node_tokens.data_ptr(), parents.data_ptr(), B, N, V,
+        res.accepted_len.data_ptr(), res.out_tokens.data_ptr(),
+        res.accepted_nodes.data_ptr() if res.accepted_nodes is not None else None,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), st.cuda_stream)
+    if status != _N.SV_OK:
+        raise _N.SpecVerifyError(status, "spec_verify_tree")
+    return res

@@ -16,6 +16,7 @@
 #include "spec_verify.h"
 #include "sv_plug.cuh"
 #include "sv_sample.cuh"
+#include "sv_tree.cuh"
 
 namespace {
 
@@ -389,6 +390,75 @@ int spec_verify_static(const void* target_logits, const void* draft_logits, int 
   return launch_both(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
                      nullptr, B, K, V, accepted_len, out_tokens, logp_out, logq_out, scratch, dc,
                      (cudaStream_t)stream);
+}
+
+size_t spec_verify_tree_workspace_bytes(int B, int N, int V, int dtype) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return 0;
+  if (B < 0 || N < 1 || N > SV_MAX_TREE_NODES || V < 1 || V > spec_verify_max_vocab(dtype)) return 0;
+  return partials_offset() + (size_t)((long long)B * (N + 1) * tiles_per_row(V, dtype)) * sizeof(float2);
+}
+
+int spec_verify_tree(const void* target_logits, int dtype, const int32_t* node_tokens,
+                     const int32_t* parents, int B, int N, int V, int32_t* accepted_len,
+                     int32_t* out_tokens, int32_t* accepted_nodes, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+  const size_t need = spec_verify_tree_workspace_bytes(B, N, V, dtype);
+  if (need == 0) return SV_ERR_SHAPE;
+  if (B == 0) return SV_OK;
+  if (!target_logits || !node_tokens || !parents || !accepted_len || !out_tokens || !workspace)
+    return SV_ERR_NULL;
+  if (!aligned_to(target_logits, (size_t)elt_of(dtype)) || !aligned_to(node_tokens, 4) ||
+      !aligned_to(parents, 4) || !aligned_to(accepted_len, 4) || !aligned_to(out_tokens, 4) ||
+      (accepted_nodes && !aligned_to(accepted_nodes, 4)) || !aligned_to(workspace, 16))
+    return SV_ERR_ALIGN;
+  if (workspace_bytes < need) return SV_ERR_WORKSPACE;
+  DeviceCache* dc = current_device_cache();
+  if (!dc) return SV_ERR_CUDA;
+  cudaStream_t st = (cudaStream_t)stream;
+  // 1. argmax partials of every target slot (every row greedy, no draft rows)
+  const bool aligned = vector_path(target_logits, target_logits, V, dtype);
+  const long long tpr = tiles_per_row(V, dtype);
+  sv::RowStatsArgs ra;
+  memset(&ra, 0, sizeof(ra));
+  ra.target = target_logits;
+  ra.draft = nullptr;
+  ra.temperature = nullptr;
+  ra.B = B;
+  ra.K = N;
+  ra.V = V;
+  ra.tiles_per_row = (int)tpr;
+  ra.n_target_rows = B * (N + 1);
+  ra.n_tiles = (long long)B * (N + 1) * tpr;   // target slots only
+  ra.k_per_row = nullptr;
+  ra.partials = (float2*)((char*)workspace + partials_offset());
+  ra.err = (unsigned*)workspace;
+  long long blocks = (long long)dc->sm_count * dc->row_stats_blocks_per_sm[dtype][aligned ? 1 : 0];
+  const long long need_blocks = (ra.n_tiles + sv::kP1Threads / 32 - 1) / (sv::kP1Threads / 32);
+  if (blocks > need_blocks) blocks = need_blocks;
+  if (blocks < 1) blocks = 1;
+  void* args1[] = {&ra};
+  if (cudaLaunchKernel(pick_row_stats(dtype, aligned), dim3((unsigned)blocks), dim3(sv::kP1Threads),
+                       args1, 0, st) != cudaSuccess)
+    return SV_ERR_CUDA;
+  // 2. one CTA per tree
+  sv::TreeArgs ta;
+  ta.node_tokens = node_tokens;
+  ta.parents = parents;
+  ta.B = B;
+  ta.N = N;
+  ta.V = V;
+  ta.tiles_per_row = (int)tpr;
+  ta.partials = ra.partials;
+  ta.err = (unsigned*)workspace;
+  ta.accepted_len = accepted_len;
+  ta.out_tokens = out_tokens;
+  ta.accepted_nodes = accepted_nodes;
+  void* args2[] = {&ta};
+  return cudaLaunchKernel((void*)sv::sv_tree_kernel, dim3((unsigned)B), dim3(sv::kP2Threads), args2,
+                          0, st) == cudaSuccess
+             ? SV_OK
+             : SV_ERR_CUDA;
 }
 
 int spec_verify_plug(const int32_t* accepted_len, const int32_t* out_tokens, int B, int K,

@@ -31,7 +31,7 @@ constexpr int kP1Threads = 256;
 struct RowStatsArgs {
   const void* target;
   const void* draft;
-  const float* temperature;
+  const float* temperature;   // [B], or nullptr: every row greedy (T = 0)
   int B, K, V;
   int tiles_per_row;
   long long n_tiles;          // (B*(K+1) + B*K) * tiles_per_row
@@ -181,7 +181,7 @@ struct WarpRows {
   __device__ __forceinline__ float T_of(int row) const {   // warp-uniform call
     const int d = row - row0;
     const float t = __shfl_sync(0xffffffffu, T_lane, d & 31);
-    return d < 32 ? t : __ldg(a->temperature + batch_of(row));
+    return d < 32 ? t : (a->temperature ? __ldg(a->temperature + batch_of(row)) : 0.f);
   }
   // Is the row read?  Target rows 0..K_b and, for T > 0, draft rows
   // 0..K_b-1 of a batch row with a valid temperature and 0 <= K_b <= K.
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kP1Threads, 4) sv_row_stats_kernel(RowStatsArg
   const int row_last = (int)((t1 - 1) / tpr);
   const bool lane_row = wr.row0 + lane <= row_last;
   const int lane_b = lane_row ? wr.batch_of(wr.row0 + lane) : 0;
-  wr.T_lane = lane_row ? __ldg(a.temperature + lane_b) : 0.f;
+  wr.T_lane = (lane_row && a.temperature) ? __ldg(a.temperature + lane_b) : 0.f;
   wr.kb_lane = lane_row ? wr.kb_of_batch(lane_b) : 0;
   wr.act_mask = __ballot_sync(0xffffffffu,
                               lane_row && wr.row_read(wr.row0 + lane, wr.T_lane, wr.kb_lane));

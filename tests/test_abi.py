@@ -160,3 +160,26 @@ def test_plug_entry_point_checks_arguments(N):
         assert call(**{field: None}) == N.SV_ERR_NULL, field
     assert call(tok=FAKE + 2) == N.SV_ERR_ALIGN
     assert call(flags=FAKE + 1) == N.SV_ERR_ALIGN
+
+
+def test_tree_entry_points_check_arguments(N):
+    B, Nn, V = 64, 21, 128256
+    tiles = -(-V // 1024)
+    assert N.spec_verify_tree_workspace_bytes(B, Nn, V, N.SV_BF16) == 256 + B * (Nn + 1) * tiles * 8
+    assert N.spec_verify_tree_workspace_bytes(B, 0, V, N.SV_BF16) == 0
+    assert N.spec_verify_tree_workspace_bytes(B, N.SV_MAX_TREE_NODES + 1, V, N.SV_BF16) == 0
+
+    def call(**kw):
+        a = dict(t=FAKE, dt=N.SV_BF16, tok=FAKE, par=FAKE, B=2, n=4, V=1024, acc=FAKE, out=FAKE,
+                 nodes=None, ws=FAKE, wsb=1 << 30)
+        a.update(kw)
+        return N.spec_verify_tree_raw(a["t"], a["dt"], a["tok"], a["par"], a["B"], a["n"], a["V"],
+                                      a["acc"], a["out"], a["nodes"], a["ws"], a["wsb"], None)
+    assert call(dt=7) == N.SV_ERR_DTYPE
+    assert call(n=0) == N.SV_ERR_SHAPE
+    assert call(B=0, t=None, tok=None, par=None, acc=None, out=None, ws=None) == N.SV_OK
+    for f in ("t", "tok", "par", "acc", "out", "ws"):
+        assert call(**{f: None}) == N.SV_ERR_NULL, f
+    assert call(t=FAKE + 1) == N.SV_ERR_ALIGN
+    assert call(nodes=FAKE + 2) == N.SV_ERR_ALIGN
+    assert call(wsb=16) == N.SV_ERR_WORKSPACE
