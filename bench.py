@@ -211,7 +211,9 @@ def run_reference(args):
 
     def step(i):
         r = [(2 * i + k) % w.B for k in range(rows_per_step)]
-        if w.k_per_row is not None:
+        if w.parents is not None:
+            oracle.verify_tree_greedy(w.target[r], w.draft_tokens[r], w.parents[r], dtype=w.dtype)
+        elif w.k_per_row is not None:
             oracle.spec_verify_ragged(w.target[r], w.draft[r], w.draft_tokens[r], w.uniforms[r],
                                       w.temperature[r], w.k_per_row[r], dtype=w.dtype)
         else:
@@ -393,6 +395,23 @@ def run_ours(args):
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = d2h_acc.numel() * 4 + d2h_tok.numel() * 4
 
+    # ---- the plug step (append the emitted tokens on the device), timed alone
+    max_len = 4096
+    seqs = torch.zeros(B, max_len, dtype=torch.int32, device=dev)
+    lens = torch.zeros(B, dtype=torch.int32, device=dev)
+    n_plug = 50
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    p0.record(stream)
+    for _ in range(n_plug):
+        if N.spec_verify_plug_raw(acc.data_ptr(), outt.data_ptr(), B, K, seqs.data_ptr(),
+                                  lens.data_ptr(), max_len, None, None, sh) != N.SV_OK:
+            raise RuntimeError("plug failed")
+    p1.record(stream)
+    barrier()
+    plug_us = p0.elapsed_time(p1) / n_plug * 1e3
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -446,6 +465,7 @@ def run_ours(args):
         "gpu_launches": gpu_launches,
         "clocks": clocks,
         "extra": {"rows_per_s": B * world / (ms_per_step * 1e-3),
+                  "plug_us_per_call": plug_us,
                   "emitted_tokens_per_step": int((accepted + 1).sum()),
                   "mean_accepted_len": float(accepted.mean()),
                   "peak_nominal_gbs": 8000.0, "frac_of_nominal": step_gbs / 8000.0},
@@ -506,10 +526,174 @@ def kernel_rev(kernel="sv_row_stats_kernel"):
     return h.hexdigest()[:12]
 
 
+def run_tree(args):
+    """Greedy tree verification (spec_verify_tree) on a tree workload: the
+    streaming kernel over the N+1 target slots of every tree, then one CTA
+    per tree.  Same timing rules as run_ours; the roofline is the step."""
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_verification_25_gb300 import _native as N
+    from speculative_decoding_verification_25_gb300 import api, synth
+    from speculative_decoding_verification_25_gb300 import build as b
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("gloo")
+    b.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synth.make(args.workload, seed=rank_seed(args.seed, rank), workers=synth.default_workers())
+    dtc = N.SV_BF16 if w.dtype == "bf16" else N.SV_F32
+    B, Nn, V = w.B, w.K, w.V
+    raw = torch.from_numpy(w.target.view(np.int16) if w.dtype == "bf16" else w.target)
+    if w.dtype == "bf16":
+        raw = raw.view(torch.bfloat16)
+    host = dict(target=raw.pin_memory(), tokens=torch.from_numpy(w.draft_tokens).pin_memory(),
+                parents=torch.from_numpy(w.parents).pin_memory())
+    copies = [{k: v.to(dev) for k, v in host.items()} for _ in range(args.copies)]
+    wsb = N.spec_verify_tree_workspace_bytes(B, Nn, V, dtc)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty(B, Nn + 1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(c):
+        st = N.spec_verify_tree_raw(c["target"].data_ptr(), dtc, c["tokens"].data_ptr(),
+                                    c["parents"].data_ptr(), B, Nn, V, acc.data_ptr(),
+                                    out.data_ptr(), None, ws.data_ptr(), wsb, stream.cuda_stream)
+        if st != N.SV_OK:
+            raise N.SpecVerifyError(st, "spec_verify_tree")
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+
+    for i in range(args.warmup):
+        call(copies[i % len(copies)])
+    sampler = ClockSampler(local)
+    sampler.start()
+    clock_t0 = time.perf_counter()
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        call(copies[i % len(copies)])
+    ev1.record(stream)
+    barrier()
+    t_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    accepted = acc.cpu().numpy()
+    i = 0
+    while time.perf_counter() - clock_t0 < 1.5:
+        call(copies[i % len(copies)])
+        i += 1
+        if i % 200 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+
+    d_acc = torch.empty(B, dtype=torch.int32).pin_memory()
+    d_out = torch.empty(B, Nn + 1, dtype=torch.int32).pin_memory()
+    dst = copies[0]
+    e2e_steps = max(10, min(args.steps, 100))
+
+    def e2e_step():
+        for k in host:
+            dst[k].copy_(host[k], non_blocking=True)
+        r = api.verify_tree(dst["target"], dst["tokens"], dst["parents"], workspace=ws)
+        d_acc.copy_(r.accepted_len, non_blocking=True)
+        d_out.copy_(r.out_tokens, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    ms_per_step = t_ms / args.steps
+    positions = B * (Nn + 1) * world            # target slots checked
+    bytes_step = B * (Nn + 1) * V * w.elt       # every slot read once, nothing re-read
+    hbm, peak_src = peaks()
+    gbs = bytes_step / (ms_per_step * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline_tree(w)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    line = {
+        "metric": METRIC, "value": positions / (ms_per_step * 1e-3), "unit": "positions/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload} B={B} N={Nn} nodes V={V} {w.dtype} logits",
+                   "B": B, "N": Nn, "V": V, "logits": w.dtype, "T": "0 (greedy tree)",
+                   "tree": "branching " + str(synth.WORKLOADS[args.workload]["tree"]),
+                   "l2": f"{len(copies)} rotating input copies of {w.target.nbytes / 1e6:.2f} MB",
+                   "parallelism": f"{world} independent replicas, own batch per GPU"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / hbm, "traffic": None,
+                     "kernel": "sv_row_stats_kernel + sv_tree_kernel (one step)",
+                     "peak_source": peak_src, "bytes_per_launch": bytes_step,
+                     "ms_per_launch": ms_per_step},
+        "cpu_baseline": cpu,
+        "e2e": {"value": positions / (e2e_ms * 1e-3), "unit": "positions/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d_acc.numel() * 4 + d_out.numel() * 4,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "extra": {"mean_accepted_depth": float(accepted.mean()),
+                  "emitted_tokens_per_step": int((accepted + 1).sum())},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _tree_job(idx):
+    from oracle import oracle
+    target, tokens, parents, dtype = _ORACLE_ROWS
+    r = [idx % len(tokens)]
+    return oracle.verify_tree_greedy(target[r], tokens[r], parents[r], dtype=dtype).accepted_len
+
+
+def cpu_baseline_tree(w, budget_s=12.0, sample_rows=4):
+    """The oracle's tree verification over a bounded sample, as cpu_baseline."""
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    rows = (w.target[:sample_rows], w.draft_tokens[:sample_rows], w.parents[:sample_rows], w.dtype)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores, initializer=_oracle_init, initargs=(rows,)) as pool:
+        pool.map(_tree_job, range(cores))
+        t0 = time.perf_counter()
+        done = 0
+        for _ in pool.imap_unordered(_tree_job, range(int(budget_s * cores * 100)), chunksize=1):
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        dt = time.perf_counter() - t0
+        pool.terminate()
+    return {"value": done * (w.K + 1) / dt, "unit": "positions/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} tree verifications cycling over rows 0..{sample_rows - 1} of the "
+                      f"{w.name} batch (N={w.K}, V={w.V}), float64 numpy, {cores} spawn workers, "
+                      f"{dt:.1f} s wall"}
+
+
 def main():
     args = parse()
+    from speculative_decoding_verification_25_gb300 import synth
+    tree = bool(synth.WORKLOADS[args.workload].get("tree"))
     if args.impl == "reference":
         run_reference(args)
+    elif tree:
+        run_tree(args)
     else:
         run_ours(args)
 

@@ -107,3 +107,12 @@ def test_stored_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     assert bench.stored_traffic("missing") is None
     monkeypatch.setattr(bench, "ROOT", real_root)
     assert set(bench.KERNEL_SOURCES) == {"sv_row_stats_kernel", "sv_accept_sample_kernel"}
+
+
+def test_tree_reference_arm_runs():
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "0", "--workload", "llama3_tree"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert res.returncode == 0, res.stderr
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
