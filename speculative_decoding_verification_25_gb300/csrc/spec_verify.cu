@@ -26,7 +26,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceCache {
   std::once_flag once;
   int sm_count = 0;
-  int row_stats_blocks_per_sm[2][2] = {{0, 0}, {0, 0}};  // [dtype][aligned]
+  int row_stats_blocks_per_sm[2][2][2] = {};  // [dtype][aligned][compact]
   cudaError_t init_error = cudaSuccess;
   // device address of g_static_scratch, looked up by the first
   // spec_verify_static call on this device
@@ -55,17 +55,24 @@ long long tiles_per_row(int V, int dtype) {
 }
 
 template <typename E, bool kAligned>
-void* row_stats_fn() {
-  return (void*)sv::sv_row_stats_kernel<E, kAligned>;
+void* row_stats_fn(bool compact) {
+  return compact ? (void*)sv::sv_row_stats_compact_kernel<E, kAligned>
+                 : (void*)sv::sv_row_stats_kernel<E, kAligned>;
 }
 template <typename E, bool kAligned>
 void* accept_fn() {
   return (void*)sv::sv_accept_sample_kernel<E, kAligned>;
 }
 
-void* pick_row_stats(int dtype, bool aligned) {
-  if (dtype == SV_BF16) return aligned ? row_stats_fn<sv::Bf16, true>() : row_stats_fn<sv::Bf16, false>();
-  return aligned ? row_stats_fn<sv::F32, true>() : row_stats_fn<sv::F32, false>();
+// compact: the kernel that splits only the rows read (verified lengths given,
+// B <= kCompactMaxB)
+void* pick_row_stats(int dtype, bool aligned, bool compact) {
+  if (dtype == SV_BF16)
+    return aligned ? row_stats_fn<sv::Bf16, true>(compact) : row_stats_fn<sv::Bf16, false>(compact);
+  return aligned ? row_stats_fn<sv::F32, true>(compact) : row_stats_fn<sv::F32, false>(compact);
+}
+bool use_compact(const int32_t* k_per_row, int B) {
+  return k_per_row != nullptr && B <= sv::kCompactMaxB;
 }
 void* pick_accept(int dtype, bool aligned) {
   if (dtype == SV_BF16) return aligned ? accept_fn<sv::Bf16, true>() : accept_fn<sv::Bf16, false>();
@@ -87,10 +94,12 @@ DeviceCache* device_cache(int dev) {
     cudaError_t e = cudaDeviceGetAttribute(&dc.sm_count, cudaDevAttrMultiProcessorCount, dev);
     for (int dt = 0; dt < 2 && e == cudaSuccess; ++dt) {
       for (int al = 0; al < 2 && e == cudaSuccess; ++al) {
-        int nb = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, pick_row_stats(dt, al != 0),
-                                                          sv::kP1Threads, 0);
-        dc.row_stats_blocks_per_sm[dt][al] = nb > 0 ? nb : 1;
+        for (int cp = 0; cp < 2 && e == cudaSuccess; ++cp) {
+          int nb = 0;
+          e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, pick_row_stats(dt, al != 0, cp != 0),
+                                                            sv::kP1Threads, 0);
+          dc.row_stats_blocks_per_sm[dt][al][cp] = nb > 0 ? nb : 1;
+        }
         void* ac = pick_accept(dt, al != 0);
         if (e == cudaSuccess)
           e = cudaFuncSetAttribute(ac, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -187,12 +196,14 @@ int launch_row_stats(const void* target_logits, const void* draft_logits, int dt
   // persistent grid: every SM filled once; every warp a contiguous tile range
   const int threads = sv::kP1Threads;
   const int warps_per_block = threads / 32;
-  long long blocks = (long long)dc->sm_count * dc->row_stats_blocks_per_sm[dtype][aligned ? 1 : 0];
+  const bool compact = use_compact(k_per_row, B);
+  long long blocks =
+      (long long)dc->sm_count * dc->row_stats_blocks_per_sm[dtype][aligned ? 1 : 0][compact ? 1 : 0];
   const long long need = (ra.n_tiles + warps_per_block - 1) / warps_per_block;
   if (blocks > need) blocks = need;
   if (blocks < 1) blocks = 1;
   void* args[] = {&ra};
-  return cudaLaunchKernel(pick_row_stats(dtype, aligned), dim3((unsigned)blocks), dim3(threads),
+  return cudaLaunchKernel(pick_row_stats(dtype, aligned, compact), dim3((unsigned)blocks), dim3(threads),
                           args, 0, st) == cudaSuccess
              ? SV_OK
              : SV_ERR_CUDA;
@@ -433,12 +444,12 @@ int spec_verify_tree(const void* target_logits, int dtype, const int32_t* node_t
   ra.k_per_row = nullptr;
   ra.partials = (float2*)((char*)workspace + partials_offset());
   ra.err = (unsigned*)workspace;
-  long long blocks = (long long)dc->sm_count * dc->row_stats_blocks_per_sm[dtype][aligned ? 1 : 0];
+  long long blocks = (long long)dc->sm_count * dc->row_stats_blocks_per_sm[dtype][aligned ? 1 : 0][0];
   const long long need_blocks = (ra.n_tiles + sv::kP1Threads / 32 - 1) / (sv::kP1Threads / 32);
   if (blocks > need_blocks) blocks = need_blocks;
   if (blocks < 1) blocks = 1;
   void* args1[] = {&ra};
-  if (cudaLaunchKernel(pick_row_stats(dtype, aligned), dim3((unsigned)blocks), dim3(sv::kP1Threads),
+  if (cudaLaunchKernel(pick_row_stats(dtype, aligned, false), dim3((unsigned)blocks), dim3(sv::kP1Threads),
                        args1, 0, st) != cudaSuccess)
     return SV_ERR_CUDA;
   // 2. one CTA per tree

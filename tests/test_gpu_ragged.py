@@ -95,3 +95,28 @@ def test_bad_lengths_are_error_rows_with_a_flag():
     assert (r.out_tokens.cpu().numpy()[:2] == -1).all()
     assert acc[2] >= 0 and acc[3] == 0
     assert api.device_errors(ws) & N.SV_DEV_BAD_K
+
+
+@pytest.mark.parametrize("B,dtype", [(2048, "f32"), (2049, "bf16")])
+def test_batch_at_and_past_the_compact_limit(B, dtype):
+    # up to 2048 batch rows the streaming pass splits only the rows read;
+    # past that every warp takes a fixed share of all rows
+    rng = np.random.default_rng(B)
+    K, V = 3, 600
+    w = _random(rng, B, K, V, dtype, rng.integers(0, K + 1, B))
+    g = run_gpu(w)
+    ref = run_oracle(w)
+    assert (g["accepted"] <= w.k_per_row).all()
+    _assert_parity(compare(ref, g["accepted"], g["out_tokens"], g["logp"], g["logq"], w.temperature))
+
+
+def test_greedy_rows_without_lengths_skip_their_draft_rows():
+    # without verified lengths every warp takes a fixed share of all rows and
+    # skips the draft rows of greedy rows inside it
+    rng = np.random.default_rng(11)
+    w = _random(rng, 40, 5, 5000, "bf16", np.full(40, 5))
+    w = dataclasses.replace(w, k_per_row=None)
+    assert (w.temperature == 0).any() and (w.temperature > 0).any()
+    g = run_gpu(w)
+    ref = run_oracle(w)
+    _assert_parity(compare(ref, g["accepted"], g["out_tokens"], g["logp"], g["logq"], w.temperature))
