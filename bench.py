@@ -435,7 +435,8 @@ def run_ours(args):
         # both kernels as one step (ragged rows)
         roofline = {"bound": "hbm", "achieved": step_gbs, "peak": hbm, "unit": "GB/s",
                     "frac": step_gbs / hbm, "traffic": None,
-                    "kernel": "sv_row_stats_kernel + sv_accept_sample_kernel (one step)",
+                    "kernel": ("sv_row_stats_compact_kernel" if w.B <= 2048 else "sv_row_stats_kernel")
+                              + " + sv_accept_sample_kernel (one step)",
                     "peak_source": peak_src, "bytes_per_launch": p1_bytes + p2_bytes,
                     "ms_per_launch": ms_per_step}
     cpu = None
