@@ -341,23 +341,35 @@ def run_ours(args):
     clocks = sampler.stop()
 
     # ---- per-kernel durations: the two stages with an event between them
-    # (the stage entry points verify every row at K, so a ragged workload
-    # reports the step instead)
-    n_split = 0 if ragged else max(args.steps, 50)
+    n_split = max(args.steps, 50)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in range(n_split)]
     barrier()
     for i in range(n_split):
         c = copies[i % len(copies)]
         evs[i][0].record(stream)
-        st = N.spec_verify_row_stats_raw(c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
-                                         c["temperature"].data_ptr(), B, K, V, ws.data_ptr(),
-                                         ws_bytes, sh)
+        if ragged:
+            st = N.spec_verify_ragged_row_stats_raw(
+                c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
+                c["temperature"].data_ptr(), c["k_per_row"].data_ptr(), B, K, V, ws.data_ptr(),
+                ws_bytes, sh)
+        else:
+            st = N.spec_verify_row_stats_raw(c["target"].data_ptr(), c["draft"].data_ptr(),
+                                             dtype_code, c["temperature"].data_ptr(), B, K, V,
+                                             ws.data_ptr(), ws_bytes, sh)
         evs[i][1].record(stream)
-        st |= N.spec_verify_accept_sample_raw(
-            c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code, c["draft_tokens"].data_ptr(),
-            c["uniforms"].data_ptr(), c["temperature"].data_ptr(), B, K, V, acc.data_ptr(),
-            outt.data_ptr(), None, None, ws.data_ptr(), ws_bytes, sh)
+        if ragged:
+            st |= N.spec_verify_ragged_accept_sample_raw(
+                c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
+                c["draft_tokens"].data_ptr(), c["uniforms"].data_ptr(),
+                c["temperature"].data_ptr(), c["k_per_row"].data_ptr(), B, K, V, acc.data_ptr(),
+                outt.data_ptr(), None, None, ws.data_ptr(), ws_bytes, sh)
+        else:
+            st |= N.spec_verify_accept_sample_raw(
+                c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
+                c["draft_tokens"].data_ptr(), c["uniforms"].data_ptr(),
+                c["temperature"].data_ptr(), B, K, V, acc.data_ptr(), outt.data_ptr(), None, None,
+                ws.data_ptr(), ws_bytes, sh)
         evs[i][2].record(stream)
         if st:
             raise RuntimeError("stage call failed")
@@ -424,21 +436,14 @@ def run_ours(args):
     p1_bytes, p2_bytes = algorithmic_bytes(w, accepted)
     hbm, peak_src = peaks()
     step_gbs = (p1_bytes + p2_bytes) / (ms_per_step * 1e-3) / 1e9
-    if k1_ms is not None:
-        # the streaming kernel, timed on its own
-        k1_gbs = p1_bytes / (k1_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": k1_gbs, "peak": hbm, "unit": "GB/s",
-                    "frac": k1_gbs / hbm, "traffic": stored_traffic(args.workload),
-                    "kernel": "sv_row_stats_kernel", "peak_source": peak_src,
-                    "bytes_per_launch": p1_bytes, "ms_per_launch": k1_ms}
-    else:
-        # both kernels as one step (ragged rows)
-        roofline = {"bound": "hbm", "achieved": step_gbs, "peak": hbm, "unit": "GB/s",
-                    "frac": step_gbs / hbm, "traffic": None,
-                    "kernel": ("sv_row_stats_compact_kernel" if w.B <= 2048 else "sv_row_stats_kernel")
-                              + " + sv_accept_sample_kernel (one step)",
-                    "peak_source": peak_src, "bytes_per_launch": p1_bytes + p2_bytes,
-                    "ms_per_launch": ms_per_step}
+    # the streaming kernel, timed on its own (verified lengths on at most
+    # 2048 rows run its compact instantiation)
+    k1_name = "sv_row_stats_compact_kernel" if ragged and B <= 2048 else "sv_row_stats_kernel"
+    k1_gbs = p1_bytes / (k1_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": k1_gbs, "peak": hbm, "unit": "GB/s",
+                "frac": k1_gbs / hbm, "traffic": stored_traffic(args.workload, k1_name),
+                "kernel": k1_name, "peak_source": peak_src,
+                "bytes_per_launch": p1_bytes, "ms_per_launch": k1_ms}
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
@@ -487,11 +492,11 @@ def describe_temperatures(T):
     return body + (f", {greedy} greedy rows" if greedy else "")
 
 
-def stored_traffic(workload):
-    """DRAM bytes per launch of the streaming kernel from the committed ncu
-    summary of this workload, or None when the summary was taken on other
-    kernel sources (or is missing)."""
-    path = os.path.join(ROOT, "profiles", f"sv_row_stats_kernel_{workload}.md")
+def stored_traffic(workload, kernel="sv_row_stats_kernel"):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu summary of
+    this workload, or None when the summary was taken on other kernel
+    sources (or is missing)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     fields = {}
@@ -500,7 +505,7 @@ def stored_traffic(workload):
             if line.startswith("- ") and ":" in line:
                 k, v = line[2:].split(":", 1)
                 fields[k.strip()] = v.strip()
-    if fields.get("kernel_rev") != kernel_rev():
+    if fields.get("kernel_rev") != kernel_rev(kernel):
         return None
     try:
         return int(fields["dram_bytes_per_launch"])
@@ -512,6 +517,7 @@ def stored_traffic(workload):
 # they are unchanged)
 KERNEL_SOURCES = {
     "sv_row_stats_kernel": ("sv_common.cuh", "sv_stream.cuh"),
+    "sv_row_stats_compact_kernel": ("sv_common.cuh", "sv_stream.cuh"),
     "sv_accept_sample_kernel": ("sv_common.cuh", "sv_stream.cuh", "sv_sample.cuh", "exp2_table.inc"),
 }
 

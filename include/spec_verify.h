@@ -164,9 +164,9 @@ int spec_verify_ragged(const void* target_logits, const void* draft_logits, int 
  * spec_verify_accept_sample folds those partials into per-position
  * statistics, runs the acceptance test and draws the replacement or bonus
  * token (re-reading only the logit rows of the one position that needs a
- * draw).  It is launched so that it may start while the previous kernel on
- * the stream drains; it must follow spec_verify_row_stats on that stream.
- * Arguments and return codes are those of spec_verify.
+ * draw).  It must follow spec_verify_row_stats on the same stream (or be
+ * ordered after it by an event).  Arguments and return codes are those of
+ * spec_verify.
  */
 int spec_verify_row_stats(const void* target_logits, const void* draft_logits, int dtype,
                           const float* temperature, int B, int K, int V,
@@ -178,6 +178,27 @@ int spec_verify_accept_sample(const void* target_logits, const void* draft_logit
                               int32_t* accepted_len, int32_t* out_tokens,
                               float* logp_out, float* logq_out,
                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The same two stages for adaptive verification (spec_verify_ragged's rule
+ * and arguments; k_per_row as there).  spec_verify_ragged_row_stats streams
+ * only the rows that the lengths select: target rows 0..K_b and, for T > 0,
+ * draft rows 0..K_b-1.  spec_verify_ragged_accept_sample must be given the
+ * same k_per_row.  Run back to back on one stream and workspace, they give
+ * exactly spec_verify_ragged's result.
+ */
+int spec_verify_ragged_row_stats(const void* target_logits, const void* draft_logits, int dtype,
+                                 const float* temperature, const int32_t* k_per_row,
+                                 int B, int K, int V,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+int spec_verify_ragged_accept_sample(const void* target_logits, const void* draft_logits,
+                                     int dtype, const int32_t* draft_tokens,
+                                     const float* uniforms, const float* temperature,
+                                     const int32_t* k_per_row, int B, int K, int V,
+                                     int32_t* accepted_len, int32_t* out_tokens,
+                                     float* logp_out, float* logq_out,
+                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Reads the device-side row flags (SV_DEV_*) that the last spec_verify call

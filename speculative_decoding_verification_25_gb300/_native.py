@@ -53,6 +53,10 @@ _SIG = {
     "spec_verify_plug": (_I, [_P, _P, _I, _I, _P, _P, _I, _P, _P, _P]),
     "spec_verify_ragged": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P,
                                 ctypes.c_size_t, _P]),
+    "spec_verify_ragged_row_stats": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _P, ctypes.c_size_t,
+                                          _P]),
+    "spec_verify_ragged_accept_sample": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P,
+                                              _P, _P, ctypes.c_size_t, _P]),
     "spec_verify_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -130,6 +134,23 @@ def spec_verify_ragged_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_pt
                                          temperature_ptr, k_per_row_ptr, B, K, V, accepted_ptr,
                                          out_tokens_ptr, logp_ptr, logq_ptr, workspace_ptr,
                                          workspace_bytes, stream_handle))
+
+
+def spec_verify_ragged_row_stats_raw(target_ptr, draft_ptr, dtype, temperature_ptr, k_per_row_ptr,
+                                     B, K, V, workspace_ptr, workspace_bytes, stream_handle) -> int:
+    return int(load().spec_verify_ragged_row_stats(target_ptr, draft_ptr, dtype, temperature_ptr,
+                                                   k_per_row_ptr, B, K, V, workspace_ptr,
+                                                   workspace_bytes, stream_handle))
+
+
+def spec_verify_ragged_accept_sample_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr,
+                                         temperature_ptr, k_per_row_ptr, B, K, V, accepted_ptr,
+                                         out_tokens_ptr, logp_ptr, logq_ptr, workspace_ptr,
+                                         workspace_bytes, stream_handle) -> int:
+    return int(load().spec_verify_ragged_accept_sample(
+        target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr, temperature_ptr, k_per_row_ptr,
+        B, K, V, accepted_ptr, out_tokens_ptr, logp_ptr, logq_ptr, workspace_ptr, workspace_bytes,
+        stream_handle))
 
 
 def spec_verify_tree_workspace_bytes(B: int, N: int, V: int, dtype: int) -> int:

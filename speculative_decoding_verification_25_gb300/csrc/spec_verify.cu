@@ -347,6 +347,39 @@ int spec_verify_accept_sample(const void* target_logits, const void* draft_logit
                               logq_out, workspace, (cudaStream_t)stream);
 }
 
+int spec_verify_ragged_row_stats(const void* target_logits, const void* draft_logits, int dtype,
+                                 const float* temperature, const int32_t* k_per_row, int B, int K,
+                                 int V, void* workspace, size_t workspace_bytes, void* stream) {
+  const int st = validate(target_logits, draft_logits, dtype, nullptr, nullptr, temperature, B, K,
+                          V, nullptr, nullptr, nullptr, nullptr, workspace, workspace_bytes, false);
+  if (st != SV_OK || B == 0) return st;
+  if (!k_per_row) return SV_ERR_NULL;
+  if (!aligned_to(k_per_row, 4)) return SV_ERR_ALIGN;
+  DeviceCache* dc = current_device_cache();
+  if (!dc) return SV_ERR_CUDA;
+  return launch_row_stats(target_logits, draft_logits, dtype, temperature, k_per_row, B, K, V,
+                          workspace, dc, (cudaStream_t)stream);
+}
+
+int spec_verify_ragged_accept_sample(const void* target_logits, const void* draft_logits,
+                                     int dtype, const int32_t* draft_tokens,
+                                     const float* uniforms, const float* temperature,
+                                     const int32_t* k_per_row, int B, int K, int V,
+                                     int32_t* accepted_len, int32_t* out_tokens, float* logp_out,
+                                     float* logq_out, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  const int st = validate(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                          B, K, V, accepted_len, out_tokens, logp_out, logq_out, workspace,
+                          workspace_bytes, true);
+  if (st != SV_OK || B == 0) return st;
+  if (!k_per_row) return SV_ERR_NULL;
+  if (!aligned_to(k_per_row, 4)) return SV_ERR_ALIGN;
+  if (!current_device_cache()) return SV_ERR_CUDA;
+  return launch_accept_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
+                              temperature, k_per_row, B, K, V, accepted_len, out_tokens, logp_out,
+                              logq_out, workspace, (cudaStream_t)stream);
+}
+
 int spec_verify(const void* target_logits, const void* draft_logits, int dtype,
                 const int32_t* draft_tokens, const float* uniforms, const float* temperature,
                 int B, int K, int V, int32_t* accepted_len, int32_t* out_tokens,

@@ -149,6 +149,24 @@ def test_ragged_entry_point_checks_its_length_array(N):
                                     None, None, FAKE, 1 << 30, None) == N.SV_ERR_DTYPE
 
 
+def test_ragged_stage_entry_points_check_their_length_array(N):
+    def rs(kpr, B=2, dt=None):
+        return N.spec_verify_ragged_row_stats_raw(FAKE, FAKE, N.SV_BF16 if dt is None else dt, FAKE,
+                                                  kpr, B, 4, 1024, FAKE, 1 << 30, None)
+
+    def acc(kpr, B=2):
+        return N.spec_verify_ragged_accept_sample_raw(FAKE, FAKE, N.SV_BF16, FAKE, FAKE, FAKE, kpr,
+                                                      B, 4, 1024, FAKE, FAKE, None, None, FAKE,
+                                                      1 << 30, None)
+    for call in (rs, acc):
+        assert call(None) == N.SV_ERR_NULL
+        assert call(FAKE + 2) == N.SV_ERR_ALIGN
+        assert call(None, B=0) == N.SV_OK
+    assert rs(FAKE, dt=9) == N.SV_ERR_DTYPE
+    assert N.spec_verify_ragged_row_stats_raw(FAKE, FAKE, N.SV_BF16, FAKE, FAKE, 2, 4, 1024, FAKE,
+                                              16, None) == N.SV_ERR_WORKSPACE
+
+
 def test_plug_entry_point_checks_arguments(N):
     def call(B=2, K=4, max_len=16, acc=FAKE, out=FAKE, tok=FAKE, L=FAKE, last=None, flags=None):
         return N.spec_verify_plug_raw(acc, out, B, K, tok, L, max_len, last, flags, None)

@@ -106,7 +106,8 @@ def test_stored_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     assert bench.stored_traffic("old") is None        # taken on other sources
     assert bench.stored_traffic("missing") is None
     monkeypatch.setattr(bench, "ROOT", real_root)
-    assert set(bench.KERNEL_SOURCES) == {"sv_row_stats_kernel", "sv_accept_sample_kernel"}
+    assert set(bench.KERNEL_SOURCES) == {"sv_row_stats_kernel", "sv_row_stats_compact_kernel",
+                                         "sv_accept_sample_kernel"}
 
 
 def test_tree_reference_arm_runs():
