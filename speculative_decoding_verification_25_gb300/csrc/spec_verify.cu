@@ -1,11 +1,15 @@
 // Host side of spec_verify: argument checks, launch geometry and the C ABI
 // declared in include/spec_verify.h.
 //
-// One call (spec_verify, spec_verify_static, or spec_verify_row_stats +
-// spec_verify_accept_sample) = two launches on the caller's stream:
+// One call (spec_verify, spec_verify_ragged, spec_verify_static, or their
+// two stage entry points) = two launches on the caller's stream:
 //   1. sv_row_stats_kernel, a persistent grid (SM count x resident CTAs)
-//      whose warps stream contiguous ranges of 2 KB row tiles;
+//      whose warps stream contiguous ranges of 2 KB row tiles; with
+//      verified lengths per row (B <= kCompactMaxB) its compact
+//      instantiation, whose warps split only the rows read;
 //   2. sv_accept_sample_kernel, one thread-block cluster per batch row.
+// spec_verify_tree runs the first kernel (target rows only) and then
+// sv_tree_kernel; spec_verify_plug is one small launch of its own.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>

@@ -12,7 +12,6 @@
 namespace sv {
 
 #define SV_NEG_INF (-__int_as_float(0x7f800000))
-static __device__ __forceinline__ float neg_inf() { return SV_NEG_INF; }
 constexpr float kFltMin = 1.17549435e-38f;
 
 // ----------------------------------------------------------------- element types
@@ -87,30 +86,8 @@ __device__ __forceinline__ void load_vec(const void* row, long long v, int V, ui
   }
 }
 
-// ----------------------------------------------------------------- async copies
-// 16-byte global -> shared copies (cp.async, L2 only) that a thread later
-// reads back itself: cp.async.wait_group makes a thread's own completed
-// copies visible to it, so no barrier is needed between the lanes.
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void lds16(uint32_t addr, uint32_t (&w)[4]) {
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-               : "r"(addr)
-               : "memory");
-}
-
 // ----------------------------------------------------------------- packed float32 pairs
-// Two float32 lanes in one 64-bit register (add/sub/mul .f32x2 on sm_100+).
+// Two float32 lanes in one 64-bit register (add and fma .f32x2 on sm_100+).
 __device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
   unsigned long long r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -118,16 +95,6 @@ __device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
 }
 __device__ __forceinline__ void f2_unpack(unsigned long long v, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
-  unsigned long long r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
-  unsigned long long r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
 }
 __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
   unsigned long long r;
@@ -167,11 +134,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ int warp_min_int(int v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ long long warp_max_ll(long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 

@@ -28,7 +28,6 @@ constexpr int kMaxGroupsPerThread = 8;
 constexpr int kMaxClusterSize = 16;
 constexpr int kBigCap = 1024;                     // large terms listed per sweep (more: evaluated inline)
 constexpr int kBigCapWarp = kBigCap / kP2Warps;   // each warp lists its own
-constexpr uint32_t kBigNone = 0xffffffffu;        // a claimed list slot that stays unused
 
 // A term whose probability exceeds this is evaluated in double-float
 // during sampling; smaller terms use the float32 path.
