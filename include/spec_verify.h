@@ -36,7 +36,12 @@
  *   - host-detectable errors return a status before anything is launched;
  *     row-level problems found on the device never fault or trap: the row is
  *     written as an error row (accepted_len = -1, all out_tokens -1) and a
- *     flag is OR-ed into the workspace (see spec_verify_device_errors).
+ *     flag is OR-ed into the workspace (see spec_verify_device_errors);
+ *   - the first call on a device fills the per-device cache (SM count,
+ *     occupancy, kernel attributes).  After one such call, spec_verify,
+ *     spec_verify_ragged and spec_verify_plug make no call that CUDA stream
+ *     capture forbids, so they may be captured into a CUDA graph and
+ *     replayed (buffers and shapes fixed at capture).
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
