@@ -39,8 +39,8 @@
  *     flag is OR-ed into the workspace (see spec_verify_device_errors);
  *   - the first call on a device fills the per-device cache (SM count,
  *     occupancy, kernel attributes).  After one such call, spec_verify,
- *     spec_verify_ragged and spec_verify_plug make no call that CUDA stream
- *     capture forbids, so they may be captured into a CUDA graph and
+ *     spec_verify_ragged, spec_verify_plug and spec_verify_and_plug make no
+ *     call that CUDA stream capture forbids, so they may be captured into a CUDA graph and
  *     replayed (buffers and shapes fixed at capture).
  */
 #ifndef SPEC_VERIFY_H
@@ -312,7 +312,8 @@ int spec_verify_tree(const void* target_logits, int dtype, const int32_t* node_t
  * [0, max_len], out_tokens[b, 0..n] goes to tokens[b, L..L+n] and seq_len[b]
  * becomes L + n + 1.  Tokens that would land at or past max_len are dropped;
  * seq_len then stops at max_len and SV_DEV_PLUG_CLIPPED is set.  Error rows
- * are left unchanged; so are rows with L outside [0, max_len], which set
+ * are left unchanged; so are rows with L outside [0, max_len] or with
+ * accepted_len[b] > K (not an output of spec_verify), which set
  * SV_DEV_BAD_LENGTH.  Enqueue it on spec_verify's stream, after the call; it
  * does not synchronise.  Returns SV_OK, SV_ERR_SHAPE (B < 0, K outside
  * [1, SV_MAX_K], max_len < 1), SV_ERR_NULL, SV_ERR_ALIGN or SV_ERR_CUDA.
@@ -320,6 +321,30 @@ int spec_verify_tree(const void* target_logits, int dtype, const int32_t* node_t
 int spec_verify_plug(const int32_t* accepted_len, const int32_t* out_tokens, int B, int K,
                      int32_t* tokens, int32_t* seq_len, int max_len, int32_t* last_token,
                      uint32_t* flags, void* stream);
+
+/*
+ * spec_verify (or spec_verify_ragged) with the plug step fused into the
+ * acceptance/sampling launch: one call, two launches, no third launch for
+ * the plug.  The thread block that writes a row's last token also appends
+ * the row's emitted tokens to `tokens` and advances `seq_len`, with exactly
+ * spec_verify_plug's rule: same arguments (tokens, seq_len, max_len,
+ * last_token), same results.  Its SV_DEV_PLUG_CLIPPED / SV_DEV_BAD_LENGTH
+ * flags go to the workspace word with the call's other device flags (read
+ * them with spec_verify_device_errors).
+ *
+ *   k_per_row  [B] int32, device, or NULL (every row verifies K).
+ * Every other argument is that of spec_verify or spec_verify_plug.  Returns
+ * spec_verify's codes, SV_ERR_SHAPE for max_len < 1, SV_ERR_NULL for a NULL
+ * tokens or seq_len, and SV_ERR_ALIGN for a misaligned int32 array.
+ */
+int spec_verify_and_plug(const void* target_logits, const void* draft_logits, int dtype,
+                         const int32_t* draft_tokens, const float* uniforms,
+                         const float* temperature, const int32_t* k_per_row,
+                         int B, int K, int V,
+                         int32_t* accepted_len, int32_t* out_tokens,
+                         float* logp_out, float* logq_out,
+                         int32_t* tokens, int32_t* seq_len, int max_len, int32_t* last_token,
+                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* spec_verify_status_string(int status);

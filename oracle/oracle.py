@@ -424,7 +424,8 @@ def plug(accepted_len, out_tokens, tokens, seq_len, last_token=None) -> PlugResu
     to L + n + 1 and last_token[b] to out_tokens[b, n].  Tokens that would
     land at or past max_len are dropped, seq_len stops at max_len and the row
     is marked clipped.  An error row (n = -1), or a row whose length lies
-    outside [0, max_len], changes nothing.
+    outside [0, max_len], changes nothing; so does n > K (out_tokens has K + 1
+    columns, so such an n is not a length the verify step writes).
     """
     tokens = np.array(tokens, np.int32, copy=True)
     seq_len = np.array(seq_len, np.int32, copy=True)
@@ -434,7 +435,7 @@ def plug(accepted_len, out_tokens, tokens, seq_len, last_token=None) -> PlugResu
     clipped = np.zeros(B, bool)
     for b in range(B):
         n = int(accepted_len[b])
-        if n < 0:
+        if n < 0 or n >= np.shape(out_tokens)[1]:
             continue
         L = int(seq_len[b])
         if L < 0 or L > max_len:

@@ -57,6 +57,8 @@ _SIG = {
                                           _P]),
     "spec_verify_ragged_accept_sample": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P,
                                               _P, _P, ctypes.c_size_t, _P]),
+    "spec_verify_and_plug": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                                  _I, _P, _P, ctypes.c_size_t, _P]),
     "spec_verify_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -151,6 +153,18 @@ def spec_verify_ragged_accept_sample_raw(target_ptr, draft_ptr, dtype, tokens_pt
         target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr, temperature_ptr, k_per_row_ptr,
         B, K, V, accepted_ptr, out_tokens_ptr, logp_ptr, logq_ptr, workspace_ptr, workspace_bytes,
         stream_handle))
+
+
+def spec_verify_and_plug_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr,
+                             temperature_ptr, k_per_row_ptr, B, K, V, accepted_ptr,
+                             out_tokens_ptr, logp_ptr, logq_ptr, seq_tokens_ptr, seq_len_ptr,
+                             max_len, last_token_ptr, workspace_ptr, workspace_bytes,
+                             stream_handle) -> int:
+    """spec_verify (ragged if k_per_row is given) with the plug step fused in."""
+    return int(load().spec_verify_and_plug(
+        target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr, temperature_ptr, k_per_row_ptr,
+        B, K, V, accepted_ptr, out_tokens_ptr, logp_ptr, logq_ptr, seq_tokens_ptr, seq_len_ptr,
+        max_len, last_token_ptr, workspace_ptr, workspace_bytes, stream_handle))
 
 
 def spec_verify_tree_workspace_bytes(B: int, N: int, V: int, dtype: int) -> int:

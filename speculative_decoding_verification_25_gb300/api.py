@@ -141,6 +141,60 @@ def plug(result: VerifyResult, tokens: torch.Tensor, seq_len: torch.Tensor, *,
         raise N.SpecVerifyError(status, "spec_verify_plug")
 
 
+def spec_verify_and_plug(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor,
+                         uniforms: torch.Tensor, temperature: torch.Tensor, tokens: torch.Tensor,
+                         seq_len: torch.Tensor, *, k_per_row: Optional[torch.Tensor] = None,
+                         last_token: Optional[torch.Tensor] = None,
+                         want_logprobs: bool = False, out: Optional[VerifyResult] = None,
+                         workspace: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None) -> VerifyResult:
+    """spec_verify followed by plug, with the plug step fused into the
+    verify call's second launch (same results as the two calls).  Plug flags
+    go to the workspace word: read them with ``device_errors(workspace)``."""
+    if target.dim() != 3:
+        raise ValueError("target must be [B, K+1, V]")
+    B, K1, V = target.shape
+    K = K1 - 1
+    dev = target.device
+    if target.dtype not in _DTYPES:
+        raise TypeError(f"target dtype {target.dtype} is not bfloat16 or float32")
+    dt = _DTYPES[target.dtype]
+    _check(target, "target", device=dev)
+    _check(draft, "draft", dtype=target.dtype, shape=(B, K, V), device=dev)
+    _check(draft_tokens, "draft_tokens", dtype=torch.int32, shape=(B, K), device=dev)
+    _check(uniforms, "uniforms", dtype=torch.float32, shape=(B, K + 1), device=dev)
+    _check(temperature, "temperature", dtype=torch.float32, shape=(B,), device=dev)
+    if tokens.dim() != 2 or tokens.shape[0] != B:
+        raise ValueError("tokens must be [B, max_len]")
+    _check(tokens, "tokens", dtype=torch.int32, device=dev)
+    _check(seq_len, "seq_len", dtype=torch.int32, shape=(B,), device=dev)
+    if last_token is not None:
+        _check(last_token, "last_token", dtype=torch.int32, shape=(B,), device=dev)
+    if k_per_row is not None:
+        _check(k_per_row, "k_per_row", dtype=torch.int32, shape=(B,), device=dev)
+    if out is None:
+        out = VerifyResult(
+            torch.empty(B, dtype=torch.int32, device=dev),
+            torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+            torch.empty(B, K, dtype=torch.float32, device=dev) if want_logprobs else None,
+            torch.empty(B, K, dtype=torch.float32, device=dev) if want_logprobs else None)
+    if workspace is None:
+        workspace = workspace_for(B, K, V, dt, dev)
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    status = N.spec_verify_and_plug_raw(
+        target.data_ptr(), draft.data_ptr(), dt, draft_tokens.data_ptr(), uniforms.data_ptr(),
+        temperature.data_ptr(), k_per_row.data_ptr() if k_per_row is not None else None, B, K, V,
+        out.accepted_len.data_ptr(), out.out_tokens.data_ptr(),
+        out.logp.data_ptr() if out.logp is not None else None,
+        out.logq.data_ptr() if out.logq is not None else None,
+        tokens.data_ptr(), seq_len.data_ptr(), tokens.shape[1],
+        last_token.data_ptr() if last_token is not None else None,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), st.cuda_stream)
+    if status != N.SV_OK:
+        raise N.SpecVerifyError(status, "spec_verify_and_plug")
+    return out
+
+
 class TreeResult(NamedTuple):
     accepted_len: torch.Tensor                  # [B] int32: depth of the accepted path, -1 = error row
     out_tokens: torch.Tensor                    # [B, N+1] int32: path tokens, bonus, -1 padded

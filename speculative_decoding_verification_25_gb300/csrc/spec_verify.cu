@@ -64,8 +64,9 @@ void* row_stats_fn(bool compact) {
                  : (void*)sv::sv_row_stats_kernel<E, kAligned>;
 }
 template <typename E, bool kAligned>
-void* accept_fn() {
-  return (void*)sv::sv_accept_sample_kernel<E, kAligned>;
+void* accept_fn(bool plug) {
+  return plug ? (void*)sv::sv_accept_sample_kernel<E, kAligned, true>
+              : (void*)sv::sv_accept_sample_kernel<E, kAligned, false>;
 }
 
 // compact: the kernel that splits only the rows read (verified lengths given,
@@ -78,9 +79,11 @@ void* pick_row_stats(int dtype, bool aligned, bool compact) {
 bool use_compact(const int32_t* k_per_row, int B) {
   return k_per_row != nullptr && B <= sv::kCompactMaxB;
 }
-void* pick_accept(int dtype, bool aligned) {
-  if (dtype == SV_BF16) return aligned ? accept_fn<sv::Bf16, true>() : accept_fn<sv::Bf16, false>();
-  return aligned ? accept_fn<sv::F32, true>() : accept_fn<sv::F32, false>();
+// plug: the instantiation with the plug step fused in
+void* pick_accept(int dtype, bool aligned, bool plug) {
+  if (dtype == SV_BF16)
+    return aligned ? accept_fn<sv::Bf16, true>(plug) : accept_fn<sv::Bf16, false>(plug);
+  return aligned ? accept_fn<sv::F32, true>(plug) : accept_fn<sv::F32, false>(plug);
 }
 
 // dynamic shared memory of the accept/sample kernel: 16 B of per-group
@@ -104,12 +107,13 @@ DeviceCache* device_cache(int dev) {
                                                             sv::kP1Threads, 0);
           dc.row_stats_blocks_per_sm[dt][al][cp] = nb > 0 ? nb : 1;
         }
-        void* ac = pick_accept(dt, al != 0);
-        if (e == cudaSuccess)
+        for (int pl = 0; pl < 2 && e == cudaSuccess; ++pl) {
+          void* ac = pick_accept(dt, al != 0, pl != 0);
           e = cudaFuncSetAttribute(ac, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)accept_smem_bytes(kMaxGroupsPerCta));
-        if (e == cudaSuccess)
-          e = cudaFuncSetAttribute(ac, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+          if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(ac, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        }
       }
     }
     dc.init_error = e;
@@ -213,11 +217,20 @@ int launch_row_stats(const void* target_logits, const void* draft_logits, int dt
              : SV_ERR_CUDA;
 }
 
+// Where the fused plug step writes (tokens == nullptr: no plug).
+struct PlugTarget {
+  int32_t* tokens = nullptr;
+  int32_t* seq_len = nullptr;
+  int32_t* last_token = nullptr;
+  int max_len = 0;
+};
+
 int launch_accept_sample(const void* target_logits, const void* draft_logits, int dtype,
                          const int32_t* draft_tokens, const float* uniforms,
                          const float* temperature, const int32_t* k_per_row, int B, int K, int V,
                          int32_t* accepted_len, int32_t* out_tokens, float* logp_out,
-                         float* logq_out, void* workspace, cudaStream_t st) {
+                         float* logq_out, void* workspace, cudaStream_t st,
+                         const PlugTarget& plug = PlugTarget()) {
   const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
   int cs, ngroups, gpc;
   cluster_geometry(V, dtype, &cs, &ngroups, &gpc);
@@ -241,6 +254,10 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
   aa.out_tokens = out_tokens;
   aa.logp_out = logp_out;
   aa.logq_out = logq_out;
+  aa.plug_tokens = plug.tokens;
+  aa.plug_seq_len = plug.seq_len;
+  aa.plug_last = plug.last_token;
+  aa.plug_max_len = plug.max_len;
   void* args[] = {&aa};
 
   cudaLaunchConfig_t cfg;
@@ -256,7 +273,8 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelExC(&cfg, pick_accept(dtype, aligned), args);
+  const cudaError_t e =
+      cudaLaunchKernelExC(&cfg, pick_accept(dtype, aligned, plug.tokens != nullptr), args);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -265,13 +283,13 @@ int launch_both(const void* target_logits, const void* draft_logits, int dtype,
                 const int32_t* draft_tokens, const float* uniforms, const float* temperature,
                 const int32_t* k_per_row, int B, int K, int V, int32_t* accepted_len,
                 int32_t* out_tokens, float* logp_out, float* logq_out, void* workspace,
-                DeviceCache* dc, cudaStream_t st) {
+                DeviceCache* dc, cudaStream_t st, const PlugTarget& plug = PlugTarget()) {
   const int r = launch_row_stats(target_logits, draft_logits, dtype, temperature, k_per_row, B, K,
                                  V, workspace, dc, st);
   if (r != SV_OK) return r;
   return launch_accept_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
                               temperature, k_per_row, B, K, V, accepted_len, out_tokens, logp_out,
-                              logq_out, workspace, st);
+                              logq_out, workspace, st, plug);
 }
 
 DeviceCache* current_device_cache() {
@@ -398,6 +416,35 @@ int spec_verify(const void* target_logits, const void* draft_logits, int dtype,
   return launch_both(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
                      nullptr, B, K, V, accepted_len, out_tokens, logp_out, logq_out, workspace, dc,
                      (cudaStream_t)stream);
+}
+
+int spec_verify_and_plug(const void* target_logits, const void* draft_logits, int dtype,
+                         const int32_t* draft_tokens, const float* uniforms,
+                         const float* temperature, const int32_t* k_per_row, int B, int K, int V,
+                         int32_t* accepted_len, int32_t* out_tokens, float* logp_out,
+                         float* logq_out, int32_t* tokens, int32_t* seq_len, int max_len,
+                         int32_t* last_token, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  const int st = validate(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                          B, K, V, accepted_len, out_tokens, logp_out, logq_out, workspace,
+                          workspace_bytes, true);
+  if (st != SV_OK) return st;
+  if (max_len < 1) return SV_ERR_SHAPE;
+  if (B == 0) return SV_OK;
+  if (!tokens || !seq_len) return SV_ERR_NULL;
+  if (!aligned_to(tokens, 4) || !aligned_to(seq_len, 4) || !aligned_to(last_token, 4) ||
+      !aligned_to(k_per_row, 4))
+    return SV_ERR_ALIGN;
+  DeviceCache* dc = current_device_cache();
+  if (!dc) return SV_ERR_CUDA;
+  PlugTarget plug;
+  plug.tokens = tokens;
+  plug.seq_len = seq_len;
+  plug.last_token = last_token;
+  plug.max_len = max_len;
+  return launch_both(target_logits, draft_logits, dtype, draft_tokens, uniforms, temperature,
+                     k_per_row, B, K, V, accepted_len, out_tokens, logp_out, logq_out, workspace,
+                     dc, (cudaStream_t)stream, plug);
 }
 
 int spec_verify_ragged(const void* target_logits, const void* draft_logits, int dtype,

@@ -23,28 +23,43 @@ struct PlugArgs {
   unsigned* flags;               // or nullptr
 };
 
-// One warp per row: lane i writes emitted token i at position L + i.
+// Plug one row with one warp.  Lane i (i <= n) holds emitted token i in
+// `tok`; n = accepted_len, so n + 1 <= SV_MAX_K + 1 <= 32 tokens.  An error
+// row (n < 0) and a length outside [0, max_len] leave the row unchanged (the
+// latter flags kDevBadLength); tokens past max_len are dropped and the
+// length stops at max_len (kDevPlugClipped).  Every lane of the warp calls it.
+__device__ __forceinline__ void plug_row(int lane, int n, int32_t tok, int32_t* seq_row,
+                                         int32_t* seq_len_b, int max_len, int32_t* last_token_b,
+                                         unsigned* flags) {
+  if (n < 0) return;
+  const int L = *seq_len_b;
+  if (L < 0 || L > max_len) {
+    if (lane == 0 && flags) atomicOr(flags, kDevBadLength);
+    return;
+  }
+  if (lane <= n && L + lane < max_len) seq_row[L + lane] = tok;
+  const int32_t last = __shfl_sync(0xffffffffu, tok, n);
+  if (lane == 0) {
+    const bool clipped = L + n + 1 > max_len;
+    *seq_len_b = clipped ? max_len : L + n + 1;
+    if (last_token_b) *last_token_b = last;
+    if (clipped && flags) atomicOr(flags, kDevPlugClipped);
+  }
+}
+
+// One warp per row.
 __global__ void __launch_bounds__(256) sv_plug_kernel(PlugArgs a) {
   const int lane = threadIdx.x & 31;
   const long long b = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (b >= a.B) return;
   const int n = a.accepted_len[b];
-  if (n < 0) return;   // error row
-  const int L = a.seq_len[b];
-  if (L < 0 || L > a.max_len) {
+  if (n > a.K) {   // not a length spec_verify writes: the row is left unchanged
     if (lane == 0 && a.flags) atomicOr(a.flags, kDevBadLength);
     return;
   }
-  const int32_t* src = a.out_tokens + b * (a.K + 1);
-  int32_t* dst = a.tokens + b * a.max_len;
-  for (int i = lane; i <= n; i += 32)
-    if (L + i < a.max_len) dst[L + i] = src[i];
-  if (lane == 0) {
-    const bool clipped = L + n + 1 > a.max_len;
-    a.seq_len[b] = clipped ? a.max_len : L + n + 1;
-    if (a.last_token) a.last_token[b] = src[n];
-    if (clipped && a.flags) atomicOr(a.flags, kDevPlugClipped);
-  }
+  const int32_t tok = (n >= 0 && lane <= n) ? a.out_tokens[b * (a.K + 1) + lane] : -1;
+  plug_row(lane, n, tok, a.tokens + b * a.max_len, a.seq_len + b, a.max_len,
+           a.last_token ? a.last_token + b : nullptr, a.flags);
 }
 
 }  // namespace sv

@@ -15,6 +15,7 @@
 
 #include <cooperative_groups.h>
 
+#include "sv_plug.cuh"
 #include "sv_stream.cuh"
 
 namespace sv {
@@ -69,6 +70,11 @@ struct AcceptArgs {
   int32_t* out_tokens;
   float* logp_out;
   float* logq_out;
+  // plug step fused into the last writes (plug_tokens == nullptr: none)
+  int32_t* plug_tokens;       // [B, plug_max_len]
+  int32_t* plug_seq_len;      // [B]
+  int32_t* plug_last;         // [B] or nullptr
+  int plug_max_len;
 };
 
 // What each CTA of a cluster publishes after its sweep.
@@ -740,9 +746,18 @@ __device__ void fold_row_stats(const AcceptArgs& a, int b, bool greedy, AcceptSm
   }
 }
 
+// The plug step for batch row b, by one warp: lane i <= n holds emitted
+// token i.
+__device__ __forceinline__ void plug_row_into(const AcceptArgs& a, int b, int lane, int n,
+                                              int32_t tok) {
+  plug_row(lane, n, tok, a.plug_tokens + (long long)b * a.plug_max_len, a.plug_seq_len + b,
+           a.plug_max_len, a.plug_last ? a.plug_last + b : nullptr, a.err);
+}
+
 // Acceptance scan (warp 0): one lane per drafted position; sets sm.n and
 // sm.bad.  With `write`, also writes accepted_len, the log-probabilities and
 // every out_tokens slot except the one a tempered row still has to sample.
+template <bool kPlug = false>
 __device__ void accept_scan(const AcceptArgs& a, int b, float T, bool write, AcceptSmem& sm) {
   const int K = a.K, lane = gtid() & 31;
   if ((gtid() >> 5) != 0) return;
@@ -781,18 +796,19 @@ __device__ void accept_scan(const AcceptArgs& a, int b, float T, bool write, Acc
       if (a.logp_out) a.logp_out[(long long)b * K + lane] = bad || greedy ? __int_as_float(0x7fffffff) : lp;
       if (a.logq_out) a.logq_out[(long long)b * K + lane] = bad || greedy ? __int_as_float(0x7fffffff) : lq;
     }
-    if (lane <= K) {
-      int v = -1;
-      if (!bad) {
-        if (lane < n) v = sm.tok[lane];
-        else if (lane == n && greedy) v = sm.rowArg[n];
-      }
-      if (!(lane == n && !greedy && !bad)) a.out_tokens[ob + lane] = v;
+    int v = -1;
+    if (!bad && lane <= K) {
+      if (lane < n) v = sm.tok[lane];
+      else if (lane == n && greedy) v = sm.rowArg[n];
     }
+    if (lane <= K && !(lane == n && !greedy && !bad)) a.out_tokens[ob + lane] = v;
     if (lane == 0) {
       a.accepted_len[b] = bad ? -1 : n;
       if (bad) atomicOr(a.err, (unsigned)bad);
     }
+    // a greedy row's tokens are all known here (a tempered row plugs after
+    // its draw; an error row is never plugged)
+    if (kPlug && greedy && !bad) plug_row_into(a, b, lane, n, v);
   }
   if (lane == 0) {
     sm.n = n;
@@ -832,7 +848,8 @@ __device__ SampleCtx sample_ctx(const AcceptArgs& a, int b, float T, int g0, int
 }
 
 // ---------------------------------------------------------------- the cluster kernel
-template <typename E, bool kAligned>
+// kPlug: the plug step is fused in (a.plug_tokens != nullptr).
+template <typename E, bool kAligned, bool kPlug>
 __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptArgs a) {
   extern __shared__ __align__(16) float4 s_part[];
   __shared__ AcceptSmem sm;
@@ -852,7 +869,7 @@ __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptA
 
   if (!sm.bad) fold_row_stats(a, b, greedy, sm);
   gsync();
-  accept_scan(a, b, T, rank == 0, sm);
+  accept_scan<kPlug>(a, b, T, rank == 0, sm);
   gsync();
   if (sm.bad || greedy) return;   // the same in every CTA of the cluster
 
@@ -881,6 +898,8 @@ __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptA
       const int token = residual ? locate<E, true>(x, sm, s_part, Wt, Qt)
                                  : locate<E, false>(x, sm, s_part, Wt, Qt);
       if (tid == 0) a.out_tokens[(long long)b * (a.K + 1) + sm.n] = token;
+      if (kPlug && tid < 32)   // warp 0 holds the token
+        plug_row_into(a, b, tid, sm.n, tid < sm.n ? sm.tok[tid] : token);
     }
     break;
   }

@@ -167,6 +167,26 @@ def test_ragged_stage_entry_points_check_their_length_array(N):
                                               16, None) == N.SV_ERR_WORKSPACE
 
 
+def test_fused_plug_entry_point_checks_arguments(N):
+    def call(**kw):
+        a = dict(t=FAKE, d=FAKE, dt=N.SV_BF16, tok=FAKE, u=FAKE, T=FAKE, kpr=None, B=2, K=4, V=1024,
+                 acc=FAKE, out=FAKE, seq=FAKE, L=FAKE, max_len=16, last=None, ws=FAKE, wsb=1 << 30)
+        a.update(kw)
+        return N.spec_verify_and_plug_raw(a["t"], a["d"], a["dt"], a["tok"], a["u"], a["T"],
+                                          a["kpr"], a["B"], a["K"], a["V"], a["acc"], a["out"],
+                                          None, None, a["seq"], a["L"], a["max_len"], a["last"],
+                                          a["ws"], a["wsb"], None)
+    assert call(B=0, seq=None, L=None) == N.SV_OK
+    assert call(max_len=0) == N.SV_ERR_SHAPE
+    assert call(seq=None) == N.SV_ERR_NULL
+    assert call(L=None) == N.SV_ERR_NULL
+    assert call(L=FAKE + 2) == N.SV_ERR_ALIGN
+    assert call(last=FAKE + 1) == N.SV_ERR_ALIGN
+    assert call(kpr=FAKE + 2) == N.SV_ERR_ALIGN
+    assert call(dt=7) == N.SV_ERR_DTYPE
+    assert call(wsb=16) == N.SV_ERR_WORKSPACE
+
+
 def test_plug_entry_point_checks_arguments(N):
     def call(B=2, K=4, max_len=16, acc=FAKE, out=FAKE, tok=FAKE, L=FAKE, last=None, flags=None):
         return N.spec_verify_plug_raw(acc, out, B, K, tok, L, max_len, last, flags, None)

@@ -20,6 +20,7 @@ def _states(rng, B, K, max_len):
     L = rng.integers(0, max_len + 1, B).astype(np.int32)
     L[:3] = [max_len - 1, max_len, 0]
     L[3:5] = [-1, max_len + 1]      # outside the buffer: left unchanged, flagged
+    acc[5:7] = [K + 1, 31]          # not a length the verify step writes: unchanged, flagged
     return acc, out, tok, L
 
 
@@ -74,3 +75,47 @@ def test_verify_then_plug_on_the_device():
     np.testing.assert_array_equal(t_tok.cpu().numpy(), want.tokens)
     np.testing.assert_array_equal(t_L.cpu().numpy(), want.seq_len)
     np.testing.assert_array_equal(last.cpu().numpy(), want.last_token)
+
+
+@pytest.mark.parametrize("name,rows", [("llama3_stochastic", range(24)), ("greedy_batch", range(32)),
+                                       ("llama3_ragged", range(24)),
+                                       ("long_draft_mixed_t", range(0, 240, 10))])
+def test_fused_plug_equals_verify_then_plug(name, rows):
+    import torch
+    from speculative_decoding_verification_25_gb300 import api, _native as N
+    w = synth.make(name, seed=2, rows=rows)
+    d = device_tensors(w)
+    if name == "llama3_stochastic":
+        d["temperature"][3] = -1.0                  # an error row: never plugged
+    B, K = w.B, w.K
+    rng = np.random.default_rng(3)
+    max_len = 3 * (K + 1)
+    tok0 = rng.integers(0, 1000, (B, max_len)).astype(np.int32)
+    L0 = rng.integers(0, max_len - K, B).astype(np.int32)
+    L0[:3] = [max_len - 1, max_len, -1]             # clipped, full, outside the buffer
+    kpr = d.get("k_per_row")
+
+    ref = api.spec_verify(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
+                          d["temperature"], k_per_row=kpr)
+    t_ref, L_ref = torch.from_numpy(tok0).cuda(), torch.from_numpy(L0).cuda()
+    last_ref = torch.full((B,), -9, dtype=torch.int32, device="cuda:0")
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    api.plug(ref, t_ref, L_ref, last_token=last_ref, flags=flags)
+
+    ws = torch.empty(N.spec_verify_workspace_bytes(B, K, w.V, N.SV_BF16 if w.dtype == "bf16"
+                                                   else N.SV_F32), dtype=torch.uint8,
+                     device="cuda:0")
+    t_f, L_f = torch.from_numpy(tok0).cuda(), torch.from_numpy(L0).cuda()
+    last_f = torch.full((B,), -9, dtype=torch.int32, device="cuda:0")
+    res = api.spec_verify_and_plug(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
+                                   d["temperature"], t_f, L_f, k_per_row=kpr, last_token=last_f,
+                                   workspace=ws)
+    dev_flags = api.device_errors(ws)
+    torch.cuda.synchronize()
+    for a, b in ((res.accepted_len, ref.accepted_len), (res.out_tokens, ref.out_tokens),
+                 (t_f, t_ref), (L_f, L_ref), (last_f, last_ref)):
+        np.testing.assert_array_equal(a.cpu().numpy(), b.cpu().numpy())
+    ref_flags = int(flags.item())
+    mask = N.SV_DEV_PLUG_CLIPPED | N.SV_DEV_BAD_LENGTH
+    assert dev_flags & mask == ref_flags & mask
+    assert ref_flags & N.SV_DEV_BAD_LENGTH and ref_flags & N.SV_DEV_PLUG_CLIPPED

@@ -54,3 +54,14 @@ def test_length_outside_the_buffer_leaves_the_row():
     r = oracle.plug(acc, out, tok, np.array([-1, 5]))
     np.testing.assert_array_equal(r.seq_len, [-1, 5])
     assert (r.tokens == 0).all() and not r.clipped.any()
+
+
+def test_length_past_the_padded_row_leaves_the_row():
+    # accepted_len above K is not an output of the verify step: nothing moves
+    acc = np.array([2, 3, 1])
+    out = np.array([[5, 6, 7], [8, 9, 10], [11, 12, -1]])
+    tok = np.zeros((3, 6), np.int32)
+    r = oracle.plug(acc, out, tok, np.array([0, 0, 0]), last_token=np.array([-5, -5, -5]))
+    np.testing.assert_array_equal(r.seq_len, [3, 0, 2])
+    np.testing.assert_array_equal(r.tokens[1], [0] * 6)
+    np.testing.assert_array_equal(r.last_token, [7, -5, 12])
