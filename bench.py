@@ -540,7 +540,8 @@ def stored_traffic(workload, kernel="sv_row_stats_kernel"):
 KERNEL_SOURCES = {
     "sv_row_stats_kernel": ("sv_common.cuh", "sv_stream.cuh"),
     "sv_row_stats_compact_kernel": ("sv_common.cuh", "sv_stream.cuh"),
-    "sv_accept_sample_kernel": ("sv_common.cuh", "sv_stream.cuh", "sv_sample.cuh", "exp2_table.inc"),
+    "sv_accept_sample_kernel": ("sv_common.cuh", "sv_stream.cuh", "sv_plug.cuh", "sv_sample.cuh",
+                                "exp2_table.inc"),
 }
 
 
