@@ -614,6 +614,13 @@ def run_tree(args):
     barrier()
     t_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     accepted = acc.cpu().numpy()
+    if args.profile:
+        sampler.stop()
+        if rank == 0:
+            print(json.dumps({"profile": True, "ms_per_step": t_ms / args.steps}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     i = 0
     while time.perf_counter() - clock_t0 < 1.5:
         call(copies[i % len(copies)])

@@ -550,7 +550,7 @@ int spec_verify_tree(const void* target_logits, int dtype, const int32_t* node_t
   ta.out_tokens = out_tokens;
   ta.accepted_nodes = accepted_nodes;
   void* args2[] = {&ta};
-  return cudaLaunchKernel((void*)sv::sv_tree_kernel, dim3((unsigned)B), dim3(sv::kP2Threads), args2,
+  return cudaLaunchKernel((void*)sv::sv_tree_kernel, dim3((unsigned)B), dim3(sv::kTreeThreads), args2,
                           0, st) == cudaSuccess
              ? SV_OK
              : SV_ERR_CUDA;

@@ -20,6 +20,8 @@ namespace sv {
 
 constexpr int kMaxTreeNodes = 128;
 constexpr unsigned kDevBadTree = 64u;
+// 32 half-warps: trees of up to 31 nodes fold every slot in one round
+constexpr int kTreeThreads = 512;
 
 struct TreeArgs {
   const int32_t* node_tokens;    // [B, N]
@@ -43,7 +45,7 @@ struct TreeSmem {
   int bad;
 };
 
-__global__ void __launch_bounds__(kP2Threads) sv_tree_kernel(TreeArgs a) {
+__global__ void __launch_bounds__(kTreeThreads) sv_tree_kernel(TreeArgs a) {
   __shared__ TreeSmem sm;
   const int b = blockIdx.x, tid = threadIdx.x;
   const int N = a.N;
@@ -56,8 +58,8 @@ __global__ void __launch_bounds__(kP2Threads) sv_tree_kernel(TreeArgs a) {
     sm.par[i] = p;
     if (t < 0 || t >= a.V || p < -1 || p >= i) atomicOr(&sm.bad, (int)kDevBadTree);
   }
-  // argmax of every slot: one half-warp per slot, 16 slots per round
-  constexpr int kHalves = kP2Threads / 16;
+  // argmax of every slot: one half-warp per slot, 32 slots per round
+  constexpr int kHalves = kTreeThreads / 16;
   const int hl = tid & 15, hw = tid >> 4;
   for (int base = 0; base <= N; base += kHalves) {   // the same trip count in every warp
     const int s = base + hw;
