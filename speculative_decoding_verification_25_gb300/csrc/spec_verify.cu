@@ -182,6 +182,29 @@ bool vector_path(const void* target_logits, const void* draft_logits, int V, int
          ((size_t)V * (size_t)elt_of(dtype)) % 16 == 0;
 }
 
+// A plain launch that may start while the preceding kernel on the stream
+// drains (programmatic dependent launch).  Only for kernels that call
+// wait_for_preceding_grid() before their first memory access; without the
+// attribute (refused) it falls back to plain stream order.
+cudaError_t launch_early(const void* fn, dim3 grid, dim3 block, void** args, cudaStream_t st) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    e = cudaLaunchKernel(fn, grid, block, args, 0, st);
+  }
+  return e;
+}
+
 int launch_row_stats(const void* target_logits, const void* draft_logits, int dtype,
                      const float* temperature, const int32_t* k_per_row, int B, int K, int V,
                      void* workspace, DeviceCache* dc, cudaStream_t st) {
@@ -211,8 +234,8 @@ int launch_row_stats(const void* target_logits, const void* draft_logits, int dt
   if (blocks > need) blocks = need;
   if (blocks < 1) blocks = 1;
   void* args[] = {&ra};
-  return cudaLaunchKernel(pick_row_stats(dtype, aligned, compact), dim3((unsigned)blocks), dim3(threads),
-                          args, 0, st) == cudaSuccess
+  return launch_early(pick_row_stats(dtype, aligned, compact), dim3((unsigned)blocks),
+                      dim3(threads), args, st) == cudaSuccess
              ? SV_OK
              : SV_ERR_CUDA;
 }
@@ -230,7 +253,7 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
                          const float* temperature, const int32_t* k_per_row, int B, int K, int V,
                          int32_t* accepted_len, int32_t* out_tokens, float* logp_out,
                          float* logq_out, void* workspace, cudaStream_t st,
-                         const PlugTarget& plug = PlugTarget()) {
+                         const PlugTarget& plug = PlugTarget(), bool early = false) {
   const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
   int cs, ngroups, gpc;
   cluster_geometry(V, dtype, &cs, &ngroups, &gpc);
@@ -266,15 +289,27 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
   cfg.blockDim = dim3(sv::kP2Threads);
   cfg.dynamicSmemBytes = accept_smem_bytes(gpc);
   cfg.stream = st;
-  cudaLaunchAttribute attrs[1];
+  cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
   attrs[0].val.clusterDim.x = (unsigned)cs;
   attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = 1;
+  // early: the grid may start as the streaming kernel's CTAs exit
+  // (programmatic dependent launch; every CTA exit is its trigger).  Only
+  // for a launch that directly follows this call's own streaming launch:
+  // the kernel reads caller inputs before it waits for the partials.
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = 1;
-  const cudaError_t e =
-      cudaLaunchKernelExC(&cfg, pick_accept(dtype, aligned, plug.tokens != nullptr), args);
+  cfg.numAttrs = early ? 2 : 1;
+  void* fn = pick_accept(dtype, aligned, plug.tokens != nullptr);
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess && early) {
+    // without the early start the dependency is plain stream order
+    (void)cudaGetLastError();
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, fn, args);
+  }
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -289,7 +324,7 @@ int launch_both(const void* target_logits, const void* draft_logits, int dtype,
   if (r != SV_OK) return r;
   return launch_accept_sample(target_logits, draft_logits, dtype, draft_tokens, uniforms,
                               temperature, k_per_row, B, K, V, accepted_len, out_tokens, logp_out,
-                              logq_out, workspace, st, plug);
+                              logq_out, workspace, st, plug, /*early=*/true);
 }
 
 DeviceCache* current_device_cache() {
@@ -533,8 +568,8 @@ int spec_verify_tree(const void* target_logits, int dtype, const int32_t* node_t
   if (blocks > need_blocks) blocks = need_blocks;
   if (blocks < 1) blocks = 1;
   void* args1[] = {&ra};
-  if (cudaLaunchKernel(pick_row_stats(dtype, aligned, false), dim3((unsigned)blocks), dim3(sv::kP1Threads),
-                       args1, 0, st) != cudaSuccess)
+  if (launch_early(pick_row_stats(dtype, aligned, false), dim3((unsigned)blocks),
+                   dim3(sv::kP1Threads), args1, st) != cudaSuccess)
     return SV_ERR_CUDA;
   // 2. one CTA per tree
   sv::TreeArgs ta;
@@ -550,8 +585,8 @@ int spec_verify_tree(const void* target_logits, int dtype, const int32_t* node_t
   ta.out_tokens = out_tokens;
   ta.accepted_nodes = accepted_nodes;
   void* args2[] = {&ta};
-  return cudaLaunchKernel((void*)sv::sv_tree_kernel, dim3((unsigned)B), dim3(sv::kTreeThreads), args2,
-                          0, st) == cudaSuccess
+  return launch_early((void*)sv::sv_tree_kernel, dim3((unsigned)B), dim3(sv::kTreeThreads), args2,
+                      st) == cudaSuccess
              ? SV_OK
              : SV_ERR_CUDA;
 }
@@ -579,8 +614,8 @@ int spec_verify_plug(const int32_t* accepted_len, const int32_t* out_tokens, int
   const long long threads = (long long)B * 32;
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   void* args[] = {&pa};
-  return cudaLaunchKernel((void*)sv::sv_plug_kernel, dim3(blocks), dim3(256), args, 0,
-                          (cudaStream_t)stream) == cudaSuccess
+  return launch_early((void*)sv::sv_plug_kernel, dim3(blocks), dim3(256), args,
+                      (cudaStream_t)stream) == cudaSuccess
              ? SV_OK
              : SV_ERR_CUDA;
 }

@@ -114,6 +114,14 @@ __device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
   return r;
 }
 
+// Wait until the preceding kernel on the stream has completed and its
+// writes are visible.  A kernel launched as a programmatic dependent may
+// start while that kernel's last CTAs drain; one launched without the
+// attribute returns from this at once.
+__device__ __forceinline__ void wait_for_preceding_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

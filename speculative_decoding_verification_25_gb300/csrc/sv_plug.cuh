@@ -49,6 +49,7 @@ __device__ __forceinline__ void plug_row(int lane, int n, int32_t tok, int32_t* 
 
 // One warp per row.
 __global__ void __launch_bounds__(256) sv_plug_kernel(PlugArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the verify step's outputs, before any access
   const int lane = threadIdx.x & 31;
   const long long b = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (b >= a.B) return;

@@ -867,6 +867,11 @@ __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptA
   gsync();
   if (sm.bad && rank != 0) return;   // row-wide, so the same in every CTA of the cluster
 
+  // Everything above reads only the caller's inputs.  Launched as a
+  // programmatic dependent of the streaming kernel, the grid may start as
+  // that kernel's CTAs exit; this waits until its partials are complete and
+  // visible (without that launch attribute it returns at once).
+  wait_for_preceding_grid();
   if (!sm.bad) fold_row_stats(a, b, greedy, sm);
   gsync();
   accept_scan<kPlug>(a, b, T, rank == 0, sm);

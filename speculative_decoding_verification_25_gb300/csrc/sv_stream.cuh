@@ -416,6 +416,7 @@ __device__ __forceinline__ void stream_compact(const RowStatsArgs& a, const int*
 
 template <typename E, bool kAligned>
 __global__ void __launch_bounds__(kP1Threads, 4) sv_row_stats_compact_kernel(RowStatsArgs a) {
+  wait_for_preceding_grid();   // before any access: the previous step may still read the workspace
   if (blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0u;
   __shared__ int s_pref[2 * kCompactMaxB + 1];
   __shared__ int s_wsum[kP1Threads / 32];
@@ -429,6 +430,7 @@ __global__ void __launch_bounds__(kP1Threads, 4) sv_row_stats_compact_kernel(Row
 
 template <typename E, bool kAligned>
 __global__ void __launch_bounds__(kP1Threads, 4) sv_row_stats_kernel(RowStatsArgs a) {
+  wait_for_preceding_grid();   // before any access: the previous step may still read the workspace
   if (blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0u;
 
   const int lane = threadIdx.x & 31;

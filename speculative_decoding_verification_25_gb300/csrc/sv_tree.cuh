@@ -46,6 +46,7 @@ struct TreeSmem {
 };
 
 __global__ void __launch_bounds__(kTreeThreads) sv_tree_kernel(TreeArgs a) {
+  wait_for_preceding_grid();   // the streaming pass's partials, before any access
   __shared__ TreeSmem sm;
   const int b = blockIdx.x, tid = threadIdx.x;
   const int N = a.N;
