@@ -33,6 +33,13 @@
  *   - work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and runs asynchronously: spec_verify never synchronises the
  *     host; inputs must stay unchanged until the stream has run the call;
+ *   - kernels are launched as programmatic dependents of the preceding
+ *     kernel on the stream, so they may be scheduled while it drains.  Each
+ *     waits (griddepcontrol.wait) for that kernel to complete before its
+ *     first memory access, except the acceptance/sampling launch of the
+ *     combined calls: it directly follows the same call's streaming launch
+ *     and reads only caller inputs before its wait.  Stream order is kept
+ *     for every read and write the caller can observe;
  *   - host-detectable errors return a status before anything is launched;
  *     row-level problems found on the device never fault or trap: the row is
  *     written as an error row (accepted_len = -1, all out_tokens -1) and a
