@@ -74,7 +74,8 @@ R15 Greedy tree verification: a node is accepted iff its parent is (or is
 R14 The plug step appends the n + 1 emitted tokens of a row at its current
     length, drops what would land past the buffer (the row is then marked
     clipped and its length stops at the buffer's end) and leaves error rows
-    unchanged.
+    unchanged; also rows whose length lies outside the buffer or whose n
+    exceeds K (not a length the verify step writes).
 """
 from __future__ import annotations
 
