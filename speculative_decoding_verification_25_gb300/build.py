@@ -1,7 +1,7 @@
 """Build libspec_verify.so in-tree with nvcc for sm_103a.
 
-One translation unit, one -gencode, no cmake: about 20 s here, well under a
-minute on the GPU host.  ``python -m speculative_decoding_verification_25_gb300.build``.
+One translation unit, one -gencode, no cmake (about 20 s of nvcc).
+``python -m speculative_decoding_verification_25_gb300.build``.
 """
 from __future__ import annotations
 
