@@ -545,14 +545,23 @@ KERNEL_SOURCES = {
 }
 
 
+def code_only(text: str) -> str:
+    """C/C++ source without comments and with whitespace runs collapsed: two
+    sources that differ only in comments or layout give the same text."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_rev(kernel="sv_row_stats_kernel"):
-    """Hash of one kernel's sources."""
+    """Hash of one kernel's sources (code only, see code_only)."""
     import hashlib
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_25_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:12]
 
 

@@ -4,7 +4,8 @@
 //   streaming kernel's partials into row statistics, runs the
 //   left-to-right acceptance test, and draws the replacement or bonus token
 //   by inverse CDF over the one position that needs it, re-reading only
-//   that position's rows.
+//   that position's rows.  The kPlug instantiation also appends each row's
+//   emitted tokens to its sequence (the plug step, sv_plug.cuh).
 //
 // The rule is the exact rejection rule of the lesson "Decodificação
 // Especulativa e EAGLE" (ai-engineering.academy, phase 10 lesson 25),

@@ -14,11 +14,15 @@
 //   the neutral partial (-inf, 0).  Draft rows of greedy rows are not read.
 //
 //   With verified lengths per row (and B <= kCompactMaxB) many rows are not
-//   read, and which ones lives on the device.  That kernel first counts, in
-//   every CTA, the rows read per segment (segment b < B: target rows of
-//   batch row b; segment B + b: its draft rows), and the warps split the
-//   tiles of those rows alone, in stacked order.  Without lengths every warp
-//   takes a fixed share of all tiles and skips the rows it need not read.
+//   read, and which ones lives on the device.  sv_row_stats_compact_kernel
+//   then first counts, in every CTA, the rows read per segment (segment
+//   b < B: target rows of batch row b; segment B + b: its draft rows), and
+//   the warps split the tiles of those rows alone, in stacked order.
+//   Without lengths (sv_row_stats_kernel) every warp takes a fixed share of
+//   all tiles and skips the rows it need not read.
+//
+//   Both kernels may be launched before the preceding kernel on the stream
+//   has finished; they wait for it before their first memory access.
 //
 // The softmax normalisers are those of the rule's p_t = softmax(target / T)
 // and q_t = softmax(draft / T) in the lesson "Decodificação Especulativa e

@@ -117,3 +117,13 @@ def test_tree_reference_arm_runs():
     assert res.returncode == 0, res.stderr
     line = json.loads(res.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
+
+
+def test_kernel_rev_ignores_comments_but_not_code():
+    sys.path.insert(0, ROOT)
+    import bench
+    a = "int f(int x) {  // doubles\n  return 2 * x; /* a\n block */ }\n"
+    b = "int f(int x) {\n  // another comment\n  return 2 * x;   }"
+    c = "int f(int x) { return 3 * x; }"
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(c)
