@@ -123,12 +123,17 @@ DeviceCache* device_cache(int dev) {
 
 // Cluster size for the sampling step: the smallest power of two for which
 // every CTA owns at most two groups per thread, at most 16 (16 needs the
-// non-portable cluster size, allowed at initialisation).
-void cluster_geometry(int V, int dtype, int* cs, int* ngroups, int* gpc) {
+// non-portable cluster size, allowed at initialisation).  Only about 33
+// clusters of 16 fit on the GPU at once, against 74 of 8, so batches of
+// more than 32 rows use clusters of 8 when a CTA can hold the larger slice
+// (at most kMaxGroupsPerCta groups): fewer waves, each paying the fixed
+// per-row chain once.
+void cluster_geometry(int V, int dtype, int B, int* cs, int* ngroups, int* gpc) {
   const int gelems = sv::kGroupVecs * vec_of(dtype);
   *ngroups = (V + gelems - 1) / gelems;
   int c = 1;
   while (c < sv::kMaxClusterSize && (*ngroups + c - 1) / c > 2 * sv::kP2Threads) c *= 2;
+  if (B > 32 && c > 8 && (*ngroups + 7) / 8 <= kMaxGroupsPerCta) c = 8;
   *cs = c;
   *gpc = (*ngroups + c - 1) / c;
 }
@@ -256,7 +261,7 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
                          const PlugTarget& plug = PlugTarget(), bool early = false) {
   const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
   int cs, ngroups, gpc;
-  cluster_geometry(V, dtype, &cs, &ngroups, &gpc);
+  cluster_geometry(V, dtype, B, &cs, &ngroups, &gpc);
   sv::AcceptArgs aa;
   aa.target = target_logits;
   aa.draft = draft_logits;
