@@ -119,3 +119,34 @@ def test_fused_plug_equals_verify_then_plug(name, rows):
     mask = N.SV_DEV_PLUG_CLIPPED | N.SV_DEV_BAD_LENGTH
     assert dev_flags & mask == ref_flags & mask
     assert ref_flags & N.SV_DEV_BAD_LENGTH and ref_flags & N.SV_DEV_PLUG_CLIPPED
+
+
+@pytest.mark.parametrize("max_len", [1, 40])
+def test_fused_plug_at_the_largest_k(max_len):
+    # K = 16: up to 17 emitted tokens per row, one per lane of the plugging warp
+    import torch
+    from speculative_decoding_verification_25_gb300 import api
+    rng = np.random.default_rng(16 + max_len)
+    B, K, V = 9, 16, 257
+    tg = rng.normal(0, 2.0, (B, K + 1, V))
+    dr = tg[:, :K] + rng.normal(0, 0.05, (B, K, V))   # close drafts: long accepted runs
+    temps = np.array([0.0, 1.0, 0.7, 1.0, 0.0, 1.3, 1.0, 0.9, 1.0], np.float32)
+    tok = np.array([[int(np.argmax(dr[b, t])) for t in range(K)] for b in range(B)], np.int32)
+    unif = rng.random((B, K + 1)).astype(np.float32)
+    w = synth.custom(tg, dr, tok, unif, temps, dtype="f32")
+    d = device_tensors(w)
+    L0 = np.array([0, 3, max_len, 0, 1, 0, 2, 0, 0], np.int32).clip(0, max_len)
+    ref = api.spec_verify(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
+                          d["temperature"])
+    t_ref = torch.full((B, max_len), -3, dtype=torch.int32, device="cuda:0")
+    L_ref = torch.from_numpy(L0).cuda()
+    api.plug(ref, t_ref, L_ref)
+    t_f = torch.full((B, max_len), -3, dtype=torch.int32, device="cuda:0")
+    L_f = torch.from_numpy(L0).cuda()
+    res = api.spec_verify_and_plug(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
+                                   d["temperature"], t_f, L_f)
+    torch.cuda.synchronize()
+    assert (ref.accepted_len.cpu().numpy() >= 8).any()   # some rows emit many tokens
+    for a, b in ((res.accepted_len, ref.accepted_len), (res.out_tokens, ref.out_tokens),
+                 (t_f, t_ref), (L_f, L_ref)):
+        np.testing.assert_array_equal(a.cpu().numpy(), b.cpu().numpy())
