@@ -112,6 +112,7 @@ struct AcceptSmem {
   int kb;   // drafted tokens this row verifies (K unless ragged)
   int redi[kP2Warps];
   CtaRecord rec;
+  CtaRecord recs[2][kMaxClusterSize];   // every CTA's record, pushed here (per attempt)
   Decision dec;
   int pick_thread;
   int pick_last;
@@ -888,13 +889,18 @@ __global__ void __launch_bounds__(kP2Threads, 4) sv_accept_sample_kernel(AcceptA
     DF Wt, Qt;
     if (residual) sweep_slice<E, kAligned, true>(x, sm, s_part, Wt, Qt);
     else sweep_slice<E, kAligned, false>(x, sm, s_part, Wt, Qt);
+    // push this CTA's record into every CTA of the cluster; after the
+    // barrier each CTA reads only its own copies, so none waits for the
+    // others to finish reading before it goes on (or exits)
+    if (tid == 0)
+      for (int r = 0; r < cs; ++r) *cluster.map_shared_rank(&sm.recs[attempt][rank], r) = sm.rec;
     cluster.sync();
-    if (tid < 32) {   // warp 0: one remote record per lane, then the decision
+    if (tid < 32) {   // warp 0: one record per lane, then the decision
       CtaRecord rec{};
-      if (tid < cs) rec = *cluster.map_shared_rank(&sm.rec, tid);
+      if (tid < cs) rec = sm.recs[attempt][tid];
       decide(rec, cs, residual, x.cw, u, a.groups_per_cta, sm);
     }
-    cluster.sync();   // every record has been read; shared memory may be reused
+    gsync();
     if (sm.dec.need_p_fallback) {
       residual = false;   // the residual is zero everywhere: draw from p_t instead
       x.rowQ = nullptr;
