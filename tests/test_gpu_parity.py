@@ -179,6 +179,8 @@ CASES = [
     (7, 4, 1000, "f32", 0), (6, 5, 4099, "bf16", 0), (5, 2, 8191, "f32", 0),
     (9, 3, 8192, "bf16", 0), (3, 6, 20000, "bf16", 1), (3, 4, 17001, "f32", 3),
     (2, 2, 65536, "bf16", 0), (2, 3, 70001, "f32", 0),
+    # V > 131072 bf16: clusters of 16 up to 32 rows, of 8 above
+    (32, 2, 140000, "bf16", 0), (33, 2, 140000, "bf16", 0),
 ]
 
 
@@ -188,7 +190,7 @@ def test_small_shapes_match_oracle(B, K, V, dtype, offset):
     temps = [0.0, 1.0, 0.3, 2.5, 0.7, 1.3, 0.0, 1.0, 0.9]
     total = None
     for variant in range(3):
-        w = _random_workload(rng, B, K, V, dtype, np.roll(temps, variant),
+        w = _random_workload(rng, B, K, V, dtype, np.resize(np.roll(temps, variant), B),
                              neg_inf=variant == 1, ties=variant == 2)
         g = run_gpu(w, offset_elems=offset)
         ref = run_oracle(w, workers=1)
