@@ -43,15 +43,21 @@ def _check(t: torch.Tensor, name: str, dtype=None, shape=None, device=None):
         raise ValueError(f"{name} must be contiguous")
 
 
-def workspace_for(B: int, K: int, V: int, dtype: int, device: torch.device) -> torch.Tensor:
-    """A cached device workspace large enough for this shape."""
+def workspace_for(B: int, K: int, V: int, dtype: int, device: torch.device,
+                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """A cached device workspace large enough for this shape, one per
+    (device, stream): calls on one stream run in order and may share it,
+    calls on different streams may overlap and must not."""
     need = N.spec_verify_workspace_bytes(B, K, V, dtype)
     if need == 0:
         raise ValueError(f"invalid shape B={B} K={K} V={V}")
-    key = (device.index if device.index is not None else torch.cuda.current_device())
+    index = device.index if device.index is not None else torch.cuda.current_device()
+    st = stream if stream is not None else torch.cuda.current_stream(index)
+    key = (index, st.cuda_stream)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < need:
-        ws = torch.empty(max(need, 1 << 20), dtype=torch.uint8, device=device)
+        with torch.cuda.stream(st):   # allocated for use on this stream
+            ws = torch.empty(max(need, 1 << 20), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
 
@@ -80,15 +86,16 @@ def spec_verify(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.T
     _check(draft_tokens, "draft_tokens", dtype=torch.int32, shape=(B, K), device=dev)
     _check(uniforms, "uniforms", dtype=torch.float32, shape=(B, K + 1), device=dev)
     _check(temperature, "temperature", dtype=torch.float32, shape=(B,), device=dev)
-    if out is None:
-        out = VerifyResult(
-            torch.empty(B, dtype=torch.int32, device=dev),
-            torch.empty(B, K + 1, dtype=torch.int32, device=dev),
-            torch.empty(B, K, dtype=torch.float32, device=dev) if want_logprobs else None,
-            torch.empty(B, K, dtype=torch.float32, device=dev) if want_logprobs else None)
-    if workspace is None:
-        workspace = workspace_for(B, K, V, dt, dev)
     st = stream if stream is not None else torch.cuda.current_stream(dev)
+    if out is None:
+        with torch.cuda.stream(st):   # outputs belong to the stream that writes them
+            out = VerifyResult(
+                torch.empty(B, dtype=torch.int32, device=dev),
+                torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                torch.empty(B, K, dtype=torch.float32, device=dev) if want_logprobs else None,
+                torch.empty(B, K, dtype=torch.float32, device=dev) if want_logprobs else None)
+    if workspace is None:
+        workspace = workspace_for(B, K, V, dt, dev, st)
     lp = out.logp.data_ptr() if out.logp is not None else None
     lq = out.logq.data_ptr() if out.logq is not None else None
     ws_bytes = workspace.numel() * workspace.element_size()
@@ -172,15 +179,16 @@ def spec_verify_and_plug(target: torch.Tensor, draft: torch.Tensor, draft_tokens
         _check(last_token, "last_token", dtype=torch.int32, shape=(B,), device=dev)
     if k_per_row is not None:
         _check(k_per_row, "k_per_row", dtype=torch.int32, shape=(B,), device=dev)
-    if out is None:
-        out = VerifyResult(
-            torch.empty(B, dtype=torch.int32, device=dev),
-            torch.empty(B, K + 1, dtype=torch.int32, device=dev),
-            torch.empty(B, K, dtype=torch.float32, device=dev) if want_logprobs else None,
-            torch.empty(B, K, dtype=torch.float32, device=dev) if want_logprobs else None)
-    if workspace is None:
-        workspace = workspace_for(B, K, V, dt, dev)
     st = stream if stream is not None else torch.cuda.current_stream(dev)
+    if out is None:
+        with torch.cuda.stream(st):   # outputs belong to the stream that writes them
+            out = VerifyResult(
+                torch.empty(B, dtype=torch.int32, device=dev),
+                torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                torch.empty(B, K, dtype=torch.float32, device=dev) if want_logprobs else None,
+                torch.empty(B, K, dtype=torch.float32, device=dev) if want_logprobs else None)
+    if workspace is None:
+        workspace = workspace_for(B, K, V, dt, dev, st)
     status = N.spec_verify_and_plug_raw(
         target.data_ptr(), draft.data_ptr(), dt, draft_tokens.data_ptr(), uniforms.data_ptr(),
         temperature.data_ptr(), k_per_row.data_ptr() if k_per_row is not None else None, B, K, V,
@@ -221,12 +229,13 @@ def verify_tree(target: torch.Tensor, node_tokens: torch.Tensor, parents: torch.
     need = _N.spec_verify_tree_workspace_bytes(B, N, V, dt)
     if need == 0:
         raise ValueError(f"invalid tree shape B={B} N={N} V={V}")
-    if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    res = TreeResult(torch.empty(B, dtype=torch.int32, device=dev),
-                     torch.empty(B, N + 1, dtype=torch.int32, device=dev),
-                     torch.empty(B, N, dtype=torch.int32, device=dev) if want_nodes else None)
     st = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.stream(st):   # blocks the allocator may reuse only after st's work
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        res = TreeResult(torch.empty(B, dtype=torch.int32, device=dev),
+                         torch.empty(B, N + 1, dtype=torch.int32, device=dev),
+                         torch.empty(B, N, dtype=torch.int32, device=dev) if want_nodes else None)
     status = _N.spec_verify_tree_raw(
         target.data_ptr(), dt, node_tokens.data_ptr(), parents.data_ptr(), B, N, V,
         res.accepted_len.data_ptr(), res.out_tokens.data_ptr(),

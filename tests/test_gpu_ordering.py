@@ -56,3 +56,34 @@ def test_inputs_written_just_before_the_call_are_seen(name):
                                       want.logp.cpu().numpy().view(np.uint32))
         np.testing.assert_array_equal(tok.cpu().numpy(), tok0.cpu().numpy())
         np.testing.assert_array_equal(L.cpu().numpy(), L0.cpu().numpy())
+
+
+def test_two_streams_with_the_default_workspace_do_not_share_it():
+    # the Python API caches one workspace per (device, stream): calls on
+    # two streams may run at the same time and must not race on scratch
+    import torch
+    from speculative_decoding_verification_25_gb300 import api
+    ws_ = [synth.make("llama3_stochastic", seed=s, rows=range(32)) for s in (11, 12)]
+    d = [device_tensors(w) for w in ws_]
+    want = []
+    for di in d:
+        r = api.spec_verify(di["target"], di["draft"], di["draft_tokens"], di["uniforms"],
+                            di["temperature"], want_logprobs=True)
+        torch.cuda.synchronize()
+        want.append((r.accepted_len.cpu().numpy(), r.out_tokens.cpu().numpy(),
+                     r.logp.cpu().numpy()))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for rnd in range(4):
+        res = []
+        for i, s in enumerate(streams):
+            with torch.cuda.stream(s):
+                di = d[i]
+                res.append(api.spec_verify(di["target"], di["draft"], di["draft_tokens"],
+                                           di["uniforms"], di["temperature"], want_logprobs=True))
+        torch.cuda.synchronize()
+        for r, (acc, out, lp) in zip(res, want):
+            np.testing.assert_array_equal(r.accepted_len.cpu().numpy(), acc)
+            np.testing.assert_array_equal(r.out_tokens.cpu().numpy(), out)
+            np.testing.assert_array_equal(r.logp.cpu().numpy().view(np.uint32), lp.view(np.uint32))
