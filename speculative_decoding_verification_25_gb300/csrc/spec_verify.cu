@@ -127,13 +127,15 @@ DeviceCache* device_cache(int dev) {
 // clusters of 16 fit on the GPU at once, against 74 of 8, so batches of
 // more than 32 rows use clusters of 8 when a CTA can hold the larger slice
 // (at most kMaxGroupsPerCta groups): fewer waves, each paying the fixed
-// per-row chain once.
-void cluster_geometry(int V, int dtype, int B, int* cs, int* ngroups, int* gpc) {
+// per-row chain once.  Likewise clusters of 8 become clusters of 4 when B
+// clusters of 8 would not all be resident at once (max_ctas = SMs x 4).
+void cluster_geometry(int V, int dtype, int B, int max_ctas, int* cs, int* ngroups, int* gpc) {
   const int gelems = sv::kGroupVecs * vec_of(dtype);
   *ngroups = (V + gelems - 1) / gelems;
   int c = 1;
   while (c < sv::kMaxClusterSize && (*ngroups + c - 1) / c > 2 * sv::kP2Threads) c *= 2;
   if (B > 32 && c > 8 && (*ngroups + 7) / 8 <= kMaxGroupsPerCta) c = 8;
+  if (c == 8 && (long long)B * 8 > max_ctas && (*ngroups + 3) / 4 <= kMaxGroupsPerCta) c = 4;
   *cs = c;
   *gpc = (*ngroups + c - 1) / c;
 }
@@ -245,6 +247,8 @@ int launch_row_stats(const void* target_logits, const void* draft_logits, int dt
              : SV_ERR_CUDA;
 }
 
+DeviceCache* current_device_cache();
+
 // Where the fused plug step writes (tokens == nullptr: no plug).
 struct PlugTarget {
   int32_t* tokens = nullptr;
@@ -261,7 +265,9 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
                          const PlugTarget& plug = PlugTarget(), bool early = false) {
   const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
   int cs, ngroups, gpc;
-  cluster_geometry(V, dtype, B, &cs, &ngroups, &gpc);
+  const DeviceCache* dc = current_device_cache();
+  const int max_ctas = dc ? dc->sm_count * 4 : 0;   // the sampling kernel's occupancy bound
+  cluster_geometry(V, dtype, B, max_ctas > 0 ? max_ctas : 1 << 30, &cs, &ngroups, &gpc);
   sv::AcceptArgs aa;
   aa.target = target_logits;
   aa.draft = draft_logits;
