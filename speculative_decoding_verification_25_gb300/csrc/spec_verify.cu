@@ -128,14 +128,17 @@ DeviceCache* device_cache(int dev) {
 // more than 32 rows use clusters of 8 when a CTA can hold the larger slice
 // (at most kMaxGroupsPerCta groups): fewer waves, each paying the fixed
 // per-row chain once.  Likewise clusters of 8 become clusters of 4 when B
-// clusters of 8 would not all be resident at once (max_ctas = SMs x 4).
-void cluster_geometry(int V, int dtype, int B, int max_ctas, int* cs, int* ngroups, int* gpc) {
+// clusters of 8 would not all be resident at once (SMs x 4 CTAs), and
+// clusters of 16 when even those give every CTA an SM of its own (a small
+// batch leaves SMs idle; halving each CTA's slice shortens the row's chain).
+void cluster_geometry(int V, int dtype, int B, int sm_count, int* cs, int* ngroups, int* gpc) {
   const int gelems = sv::kGroupVecs * vec_of(dtype);
   *ngroups = (V + gelems - 1) / gelems;
   int c = 1;
   while (c < sv::kMaxClusterSize && (*ngroups + c - 1) / c > 2 * sv::kP2Threads) c *= 2;
   if (B > 32 && c > 8 && (*ngroups + 7) / 8 <= kMaxGroupsPerCta) c = 8;
-  if (c == 8 && (long long)B * 8 > max_ctas && (*ngroups + 3) / 4 <= kMaxGroupsPerCta) c = 4;
+  if (c == 8 && (long long)B * 8 > 4LL * sm_count && (*ngroups + 3) / 4 <= kMaxGroupsPerCta) c = 4;
+  if (c == 8 && (long long)B * 16 <= sm_count) c = 16;
   *cs = c;
   *gpc = (*ngroups + c - 1) / c;
 }
@@ -266,8 +269,7 @@ int launch_accept_sample(const void* target_logits, const void* draft_logits, in
   const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
   int cs, ngroups, gpc;
   const DeviceCache* dc = current_device_cache();
-  const int max_ctas = dc ? dc->sm_count * 4 : 0;   // the sampling kernel's occupancy bound
-  cluster_geometry(V, dtype, B, max_ctas > 0 ? max_ctas : 1 << 30, &cs, &ngroups, &gpc);
+  cluster_geometry(V, dtype, B, dc && dc->sm_count > 0 ? dc->sm_count : 148, &cs, &ngroups, &gpc);
   sv::AcceptArgs aa;
   aa.target = target_logits;
   aa.draft = draft_logits;
