@@ -128,9 +128,10 @@ DeviceCache* device_cache(int dev) {
 // more than 32 rows use clusters of 8 when a CTA can hold the larger slice
 // (at most kMaxGroupsPerCta groups): fewer waves, each paying the fixed
 // per-row chain once.  Likewise clusters of 8 become clusters of 4 when B
-// clusters of 8 would not all be resident at once (SMs x 4 CTAs), and
-// clusters of 16 when even those give every CTA an SM of its own (a small
-// batch leaves SMs idle; halving each CTA's slice shortens the row's chain).
+// clusters of 8 would not all be resident at once (SMs x 4 CTAs).  A small
+// batch leaves SMs idle instead: the cluster doubles while every CTA still
+// gets an SM of its own and keeps at least 64 groups, since a smaller slice
+// shortens the row's chain.
 void cluster_geometry(int V, int dtype, int B, int sm_count, int* cs, int* ngroups, int* gpc) {
   const int gelems = sv::kGroupVecs * vec_of(dtype);
   *ngroups = (V + gelems - 1) / gelems;
@@ -138,7 +139,9 @@ void cluster_geometry(int V, int dtype, int B, int sm_count, int* cs, int* ngrou
   while (c < sv::kMaxClusterSize && (*ngroups + c - 1) / c > 2 * sv::kP2Threads) c *= 2;
   if (B > 32 && c > 8 && (*ngroups + 7) / 8 <= kMaxGroupsPerCta) c = 8;
   if (c == 8 && (long long)B * 8 > 4LL * sm_count && (*ngroups + 3) / 4 <= kMaxGroupsPerCta) c = 4;
-  if (c == 8 && (long long)B * 16 <= sm_count) c = 16;
+  while (c < sv::kMaxClusterSize && (long long)B * 2 * c <= sm_count &&
+         (*ngroups + 2 * c - 1) / (2 * c) >= 64)
+    c *= 2;
   *cs = c;
   *gpc = (*ngroups + c - 1) / c;
 }

@@ -181,8 +181,9 @@ CASES = [
     (2, 2, 65536, "bf16", 0), (2, 3, 70001, "f32", 0),
     # V > 131072 bf16: clusters of 16 up to 32 rows, of 8 above
     (32, 2, 140000, "bf16", 0), (33, 2, 140000, "bf16", 0),
-    # clusters of 8 by V, 16 while B * 16 <= 152 SMs
+    # small batches: the cluster doubles while B * 2c <= 152 SMs (>= 64 groups per CTA)
     (4, 4, 128256, "bf16", 0), (9, 3, 100000, "bf16", 0), (10, 3, 100000, "bf16", 0),
+    (1, 4, 32000, "bf16", 0), (16, 2, 32000, "bf16", 0), (3, 4, 9000, "f32", 5),
 ]
 
 
