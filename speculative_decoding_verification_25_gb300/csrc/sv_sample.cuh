@@ -317,14 +317,19 @@ __device__ void sweep_slice(const SampleCtx& x, AcceptSmem& sm, float4* part, DF
           const bool b0 = ep0 > x.thp || eq0 > x.thq;
           const bool b1 = ep1 > x.thp || eq1 > x.thq;
           big |= ((unsigned)b0 << bit) | ((unsigned)b1 << (bit + 1));
+          // a large term leaves the float32 sums: zero its e^p and e^q once
+          // (then d = 0 - cw*0 = +0 and it adds +0 everywhere, as a skip would)
+          ep0 = b0 ? 0.f : ep0;
+          ep1 = b1 ? 0.f : ep1;
+          eq0 = b0 ? 0.f : eq0;
+          eq1 = b1 ? 0.f : eq1;
+          const unsigned long long ep2 = f2_pack(ep0, ep1), eq2 = f2_pack(eq0, eq1);
           float d0, d1;
-          f2_unpack(f2_fma(ncw2, f2_pack(eq0, eq1), f2_pack(ep0, ep1)), d0, d1);
-          d0 = b0 ? 0.f : d0;
-          d1 = b1 ? 0.f : d1;
+          f2_unpack(f2_fma(ncw2, eq2, ep2), d0, d1);
           sw2 = f2_add(sw2, f2_pack(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
           sq2 = f2_add(sq2, f2_pack(d0 > 0.f ? eq0 : 0.f, d1 > 0.f ? eq1 : 0.f));
-          sp2 = f2_add(sp2, f2_pack(b0 ? 0.f : ep0, b1 ? 0.f : ep1));
-          sQ2 = f2_add(sQ2, f2_pack(b0 ? 0.f : eq0, b1 ? 0.f : eq1));
+          sp2 = f2_add(sp2, ep2);
+          sQ2 = f2_add(sQ2, eq2);
         } else {
           const bool b0 = ep0 > x.thp, b1 = ep1 > x.thp;
           big |= ((unsigned)b0 << bit) | ((unsigned)b1 << (bit + 1));
