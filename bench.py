@@ -1,16 +1,21 @@
 """Benchmark of the batched verify-and-accept step (one JSON line on rank 0).
 
-A step is one spec_verify call -- the streaming statistics pass plus the
-accept/sample pass -- over one batch of the B=64, K=4, V=128256 bf16
-workload (Zipf-like logits, T = 1), inputs resident in HBM.  Three copies of
-the inputs rotate (each 147.75 MB of logits, more than the 129 MB L2).
+A step is one spec_verify call -- one launch of the persistent kernel that
+streams every logit row, folds the statistics, runs the acceptance scan and
+draws the replacement or bonus token -- over one batch of the B=64, K=4,
+V=128256 bf16 workload (Zipf-like logits, T = 1), inputs resident in HBM.
+Input copies rotate so that every step reads data L2 has evicted (each
+copy's logits, 147.75 MB, exceed the 129 MB L2); a workload too small for
+that is timed one call at a time with an L2 flush before each.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME | --workload all]
 
 Under torchrun every rank verifies its own batch (its own seed) with no
 collective on the data path: weak scaling, value = all ranks' positions / the
 slowest rank's time.  ``--impl reference`` times the float64 CPU oracle on
-the host cores instead (rank 0 only).
+the host cores instead (rank 0 only).  ``--workload all`` prints one line for
+each of the five synthetic workloads.
 """
 from __future__ import annotations
 
@@ -151,6 +156,7 @@ class ClockSampler:
 
 
 _ORACLE_ROWS = None
+_ORACLE_CACHE = {}
 
 
 def _oracle_init(rows):
@@ -158,44 +164,75 @@ def _oracle_init(rows):
     _ORACLE_ROWS = rows
 
 
-def _oracle_job(idx):
+def _workload_init(name, seed, keep):
+    """Worker start: rebuild the rows the timing loop cycles over (the
+    generator draws every row from streams of its own)."""
+    global _ORACLE_ROWS
+    _ORACLE_ROWS = (name, seed)
+    from speculative_decoding_verification_25_gb300 import synth
+    for r in range(keep):
+        _ORACLE_CACHE[r] = synth.make(name, seed=seed, rows=[r])
+
+
+def _oracle_row(r):
     from oracle import oracle
-    target, draft, tokens, unif, temp, dtype, kpr = _ORACLE_ROWS
-    r = [idx % len(temp)]
-    if kpr is not None:
-        return oracle.spec_verify_ragged(target[r], draft[r], tokens[r], unif[r], temp[r],
-                                         kpr[r], dtype=dtype).accepted_len
-    return oracle.spec_verify(target[r], draft[r], tokens[r], unif[r], temp[r],
-                              dtype=dtype).accepted_len
+    w = _ORACLE_CACHE.get(r)
+    if w is None:
+        from speculative_decoding_verification_25_gb300 import synth
+        name, seed = _ORACLE_ROWS
+        w = synth.make(name, seed=seed, rows=[r])
+    if w.k_per_row is not None:
+        return oracle.spec_verify_ragged(w.target, w.draft, w.draft_tokens, w.uniforms,
+                                         w.temperature, w.k_per_row, dtype=w.dtype)
+    return oracle.spec_verify(w.target, w.draft, w.draft_tokens, w.uniforms, w.temperature,
+                              dtype=w.dtype)
 
 
-def cpu_baseline(w, budget_s=12.0, sample_rows=4):
-    """The float64 oracle, as it stands, on the host cores over a bounded
-    sample: the first ``sample_rows`` rows of the batch, verified over and
-    over by a spawn pool (one worker per core) for about ``budget_s``."""
+def _oracle_timed(idx):
+    return _oracle_row(idx % len(_ORACLE_CACHE)).accepted_len
+
+
+def cpu_baseline(w, seed, gpu, budget_s=12.0, keep=16):
+    """The float64 oracle, as it stands, on the host cores (one spawn worker
+    per core).  It first verifies every row of the batch once, and those
+    results give the parity counts of the GPU outputs ``gpu`` (accepted,
+    out_tokens, logp, logq); then it cycles over the first ``keep`` rows for
+    about ``budget_s`` -- the timed sample.  Returns (cpu_baseline, parity)."""
     import multiprocessing as mp
+    from oracle import oracle
+    from oracle.parity import check_structure, compare
     cores = os.cpu_count() or 1
-    kpr = getattr(w, "k_per_row", None)
-    rows = (w.target[:sample_rows], w.draft[:sample_rows], w.draft_tokens[:sample_rows],
-            w.uniforms[:sample_rows], w.temperature[:sample_rows], w.dtype,
-            None if kpr is None else kpr[:sample_rows])
-    pos_per_row = float((row_lengths(w)[:sample_rows] + 1).mean())
+    keep = min(keep, w.B)
     ctx = mp.get_context("spawn")
-    with ctx.Pool(cores, initializer=_oracle_init, initargs=(rows,)) as pool:
-        pool.map(_oracle_job, range(cores))   # warm the workers (imports)
+    with ctx.Pool(cores, initializer=_workload_init, initargs=(w.name, seed, keep)) as pool:
+        parts = pool.map(_oracle_row, range(w.B), chunksize=1)
         t0 = time.perf_counter()
         done = 0
-        for _ in pool.imap_unordered(_oracle_job, range(int(budget_s * cores * 100)), chunksize=1):
+        for _ in pool.imap_unordered(_oracle_timed, range(int(budget_s * cores * 100)), chunksize=1):
             done += 1
             if time.perf_counter() - t0 > budget_s:
                 break
         dt = time.perf_counter() - t0
         pool.terminate()
-    return {"value": done * pos_per_row / dt, "unit": "positions/s", "cores": cores,
-            "kind": "oracle",
-            "sample": f"{done} row verifications cycling over rows 0..{sample_rows - 1} of the "
-                      f"{w.name} batch (K={w.K}, V={w.V}), float64 numpy, {cores} spawn "
-                      f"workers, {dt:.1f} s wall"}
+    cat = lambda f: np.concatenate([getattr(p, f) for p in parts])
+    ref = oracle.BatchResult(cat("accepted_len"), cat("out_tokens"), cat("logp"), cat("logq"),
+                             cat("ratio_margin"), cat("cdf_margin"), sum((p.mode for p in parts), []))
+    acc, out, lp, lq = gpu
+    rep = compare(ref, acc, out, lp, lq, w.temperature)
+    parity = {"rows": rep.rows, "greedy_rows": rep.greedy_rows,
+              "stochastic_rows": rep.stochastic_rows, "ambiguous_rows": rep.ambiguous_rows,
+              "mismatched_rows": rep.mismatched_rows,
+              "mismatched_frac": rep.mismatched_rows / max(1, rep.rows),
+              "max_logprob_err": rep.max_logprob_err, "rule_failures": len(rep.failures),
+              "structure_failures": len(check_structure(acc, out, w.draft_tokens, w.V)),
+              "oracle": "float64 numpy, every row of the timed batch"}
+    pos_per_row = float((row_lengths(w)[:keep] + 1).mean())
+    cpu = {"value": done * pos_per_row / dt, "unit": "positions/s", "cores": cores,
+           "kind": "oracle",
+           "sample": f"{done} row verifications cycling over rows 0..{keep - 1} of the "
+                     f"{w.name} batch (K={w.K}, V={w.V}), float64 numpy, {cores} spawn "
+                     f"workers, {dt:.1f} s wall"}
+    return cpu, parity
 
 
 def run_reference(args):
@@ -246,12 +283,23 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+FIVE = ("tiny_stochastic", "greedy_batch", "llama3_stochastic", "long_draft_mixed_t",
+        "large_vocab_stress")
+
+
+def _json_default(o):
+    """numpy scalars in the JSON line"""
+    if isinstance(o, np.integer):
+        return int(o)
+    if isinstance(o, np.floating):
+        return float(o)
+    raise TypeError(f"not JSON serializable: {type(o).__name__}")
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
-    from speculative_decoding_verification_25_gb300 import _native as N
-    from speculative_decoding_verification_25_gb300 import api, synth
     from speculative_decoding_verification_25_gb300 import build as b
 
     rank, world, local = dist_env()
@@ -259,8 +307,26 @@ def run_ours(args):
         dist.init_process_group("gloo")
     b.build()
     torch.cuda.set_device(local)
+    names = FIVE if args.workload == "all" else (args.workload,)
+    for name in names:
+        line = bench_workload(args, name, rank, world, local)
+        if rank == 0 and line is not None:
+            print(json.dumps(line, default=_json_default), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def bench_workload(args, name, rank, world, local):
+    """Time one workload; returns the JSON line (rank 0) or None."""
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_verification_25_gb300 import _native as N
+    from speculative_decoding_verification_25_gb300 import api, synth
+
     dev = torch.device("cuda", local)
-    w = synth.make(args.workload, seed=rank_seed(args.seed, rank), workers=synth.default_workers())
+    seed = rank_seed(args.seed, rank)
+    w = synth.make(name, seed=seed, workers=synth.default_workers())
     dt_torch = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     dtype_code = N.SV_BF16 if w.dtype == "bf16" else N.SV_F32
     B, K, V = w.B, w.K, w.V
@@ -276,26 +342,36 @@ def run_ours(args):
                 temperature=torch.from_numpy(w.temperature).pin_memory())
     if ragged:
         host["k_per_row"] = torch.from_numpy(np.ascontiguousarray(w.k_per_row, np.int32)).pin_memory()
-    copies = [{k: v.to(dev) for k, v in host.items()} for _ in range(args.copies)]
+
+    # Cold inputs: the bytes touched between two uses of one copy must be at
+    # least twice the L2.  Rotate enough copies when that takes few; else
+    # time one call at a time with a flush of 2 x L2 before each.
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    p1_all, _ = algorithmic_bytes(w, np.zeros(B, np.int64))
+    need = 1 + -(-2 * l2 // max(1, p1_all))
+    rotate = need <= 64
+    n_copies = max(args.copies, need) if rotate else 1
+    copies = [{k: v.to(dev) for k, v in host.items()} for _ in range(n_copies)]
+    flush = None if rotate else torch.empty(2 * l2, dtype=torch.uint8, device=dev)
     ws_bytes = N.spec_verify_workspace_bytes(B, K, V, dtype_code)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     acc = torch.empty(B, dtype=torch.int32, device=dev)
     outt = torch.empty(B, K + 1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
-    def call(c):
+    def call(c, lp=None, lq=None):
         if ragged:
             st = N.spec_verify_ragged_raw(c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
                                           c["draft_tokens"].data_ptr(), c["uniforms"].data_ptr(),
                                           c["temperature"].data_ptr(), c["k_per_row"].data_ptr(),
-                                          B, K, V, acc.data_ptr(), outt.data_ptr(), None, None,
+                                          B, K, V, acc.data_ptr(), outt.data_ptr(), lp, lq,
                                           ws.data_ptr(), ws_bytes, sh)
         else:
             st = N.spec_verify_raw(c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
                                    c["draft_tokens"].data_ptr(), c["uniforms"].data_ptr(),
                                    c["temperature"].data_ptr(), B, K, V, acc.data_ptr(),
-                                   outt.data_ptr(), None, None, ws.data_ptr(), ws_bytes, sh)
+                                   outt.data_ptr(), lp, lq, ws.data_ptr(), ws_bytes, sh)
         if st != N.SV_OK:
             raise N.SpecVerifyError(st)
 
@@ -304,80 +380,55 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-
     # ---- warm-up, then the timed region (device events on the launching stream)
     for i in range(args.warmup):
+        if flush is not None:
+            flush.fill_(i & 0xff)
         call(copies[i % len(copies)])
     sampler = ClockSampler(local)
     sampler.start()
     clock_t0 = time.perf_counter()
     barrier()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for i in range(args.steps):
-        call(copies[i % len(copies)])
-    ev1.record(stream)
-    barrier()
-    t_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
-    gpu_launches = 2 * args.steps
+    if rotate:
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(args.steps):
+            call(copies[i % len(copies)])
+        ev1.record(stream)
+        barrier()
+        t_ms = ev0.elapsed_time(ev1)
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)          # evict the inputs from L2 (outside the events)
+            evs[i][0].record(stream)
+            call(copies[0])
+            evs[i][1].record(stream)
+        barrier()
+        t_ms = sum(a.elapsed_time(e) for a, e in evs)
+    t_ms = max_over_ranks(t_ms, world)
+    gpu_launches = args.steps
     accepted = acc.cpu().numpy()
     if args.profile:
         sampler.stop()
         if rank == 0:
-            print(json.dumps({"profile": True, "ms_per_step": t_ms / args.steps}), flush=True)
-        if world > 1:
-            dist.destroy_process_group()
-        return
+            print(json.dumps({"profile": True, "workload": name, "ms_per_step": t_ms / args.steps}),
+                  flush=True)
+        return None
 
     # keep the GPU on the same steps for >= 1.5 s so the clock samples see load
     i = 0
     while time.perf_counter() - clock_t0 < 1.5:
+        if flush is not None:
+            flush.fill_(i & 0xff)
         call(copies[i % len(copies)])
         i += 1
         if i % 200 == 0:
             torch.cuda.synchronize(dev)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
-
-    # ---- per-kernel durations: the two stages with an event between them
-    n_split = max(args.steps, 50)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True)) for _ in range(n_split)]
-    barrier()
-    for i in range(n_split):
-        c = copies[i % len(copies)]
-        evs[i][0].record(stream)
-        if ragged:
-            st = N.spec_verify_ragged_row_stats_raw(
-                c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
-                c["temperature"].data_ptr(), c["k_per_row"].data_ptr(), B, K, V, ws.data_ptr(),
-                ws_bytes, sh)
-        else:
-            st = N.spec_verify_row_stats_raw(c["target"].data_ptr(), c["draft"].data_ptr(),
-                                             dtype_code, c["temperature"].data_ptr(), B, K, V,
-                                             ws.data_ptr(), ws_bytes, sh)
-        evs[i][1].record(stream)
-        if ragged:
-            st |= N.spec_verify_ragged_accept_sample_raw(
-                c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
-                c["draft_tokens"].data_ptr(), c["uniforms"].data_ptr(),
-                c["temperature"].data_ptr(), c["k_per_row"].data_ptr(), B, K, V, acc.data_ptr(),
-                outt.data_ptr(), None, None, ws.data_ptr(), ws_bytes, sh)
-        else:
-            st |= N.spec_verify_accept_sample_raw(
-                c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
-                c["draft_tokens"].data_ptr(), c["uniforms"].data_ptr(),
-                c["temperature"].data_ptr(), B, K, V, acc.data_ptr(), outt.data_ptr(), None, None,
-                ws.data_ptr(), ws_bytes, sh)
-        evs[i][2].record(stream)
-        if st:
-            raise RuntimeError("stage call failed")
-    barrier()
-    k1 = [a.elapsed_time(m) for a, m, _ in evs]
-    k2 = [m.elapsed_time(e) for _, m, e in evs]
-    k1_ms = statistics.mean(k1) if k1 else None
-    k2_ms = statistics.mean(k2) if k2 else None
 
     # ---- end to end through the public call with host buffers
     d2h_acc = torch.empty(B, dtype=torch.int32).pin_memory()
@@ -407,7 +458,7 @@ def run_ours(args):
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = d2h_acc.numel() * 4 + d2h_tok.numel() * 4
 
-    # ---- the plug step (append the emitted tokens on the device), timed alone
+    # ---- the plug step: on its own, and fused into the verify launch
     max_len = 4096
     seqs = torch.zeros(B, max_len, dtype=torch.int32, device=dev)
     lens = torch.zeros(B, dtype=torch.int32, device=dev)
@@ -423,32 +474,38 @@ def run_ours(args):
     p1.record(stream)
     barrier()
     plug_us = p0.elapsed_time(p1) / n_plug * 1e3
+    fused_us = None
+    if rotate:
+        n_fused = max(args.steps, 50)
+        lens.zero_()
+        barrier()
+        p0.record(stream)
+        for i in range(n_fused):
+            c = copies[i % len(copies)]
+            if N.spec_verify_and_plug_raw(
+                    c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
+                    c["draft_tokens"].data_ptr(), c["uniforms"].data_ptr(),
+                    c["temperature"].data_ptr(), c["k_per_row"].data_ptr() if ragged else None,
+                    B, K, V, acc.data_ptr(), outt.data_ptr(), None, None, seqs.data_ptr(),
+                    lens.data_ptr(), max_len, None, ws.data_ptr(), ws_bytes, sh) != N.SV_OK:
+                raise RuntimeError("spec_verify_and_plug failed")
+            if (i + 1) % 64 == 0:
+                lens.zero_()
+        p1.record(stream)
+        barrier()
+        fused_us = p0.elapsed_time(p1) / n_fused * 1e3
 
-    # ---- the step with the plug fused into its second launch (rotating
-    # copies as in the timed region); lengths restart so nothing clips
-    n_fused = max(args.steps, 50)
-    lens.zero_()
-    barrier()
-    p0.record(stream)
-    for i in range(n_fused):
-        c = copies[i % len(copies)]
-        if N.spec_verify_and_plug_raw(
-                c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
-                c["draft_tokens"].data_ptr(), c["uniforms"].data_ptr(),
-                c["temperature"].data_ptr(), c["k_per_row"].data_ptr() if ragged else None, B, K,
-                V, acc.data_ptr(), outt.data_ptr(), None, None, seqs.data_ptr(), lens.data_ptr(),
-                max_len, None, ws.data_ptr(), ws_bytes, sh) != N.SV_OK:
-            raise RuntimeError("spec_verify_and_plug failed")
-        if (i + 1) % 64 == 0:
-            lens.zero_()
-    p1.record(stream)
-    barrier()
-    fused_us = p0.elapsed_time(p1) / n_fused * 1e3
+    # ---- the outputs the parity block checks (one call with log-probabilities)
+    lp = torch.empty(B, K, dtype=torch.float32, device=dev)
+    lq = torch.empty(B, K, dtype=torch.float32, device=dev)
+    call(copies[0], lp.data_ptr(), lq.data_ptr())
+    torch.cuda.synchronize(dev)
+    gpu_out = (acc.cpu().numpy(), outt.cpu().numpy(), lp.cpu().numpy(), lq.cpu().numpy())
+    dev_flags = api.device_errors(ws)
 
     if rank != 0:
-        if world > 1:
-            dist.destroy_process_group()
-        return
+        del copies, host
+        return None
 
     ms_per_step = t_ms / args.steps
     # verified positions: K_b + 1 per row (the target positions the step checks)
@@ -457,50 +514,56 @@ def run_ours(args):
     p1_bytes, p2_bytes = algorithmic_bytes(w, accepted)
     hbm, peak_src = peaks()
     step_gbs = (p1_bytes + p2_bytes) / (ms_per_step * 1e-3) / 1e9
-    # the streaming kernel, timed on its own (verified lengths on at most
-    # 2048 rows run its compact instantiation)
-    k1_name = "sv_row_stats_compact_kernel" if ragged and B <= 2048 else "sv_row_stats_kernel"
-    k1_gbs = p1_bytes / (k1_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "achieved": k1_gbs, "peak": hbm, "unit": "GB/s",
-                "frac": k1_gbs / hbm, "traffic": stored_traffic(args.workload, k1_name),
-                "kernel": k1_name, "peak_source": peak_src,
-                "bytes_per_launch": p1_bytes, "ms_per_launch": k1_ms}
-    cpu = None
+    roofline = {"bound": "hbm", "achieved": step_gbs, "peak": hbm, "unit": "GB/s",
+                "frac": step_gbs / hbm, "traffic": stored_traffic(name, "sv_fused_kernel"),
+                "kernel": "sv_fused_kernel (the whole step is this one launch)",
+                "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_src == "measured" else "fallback",
+                "bytes_per_launch": p1_bytes + p2_bytes,
+                "bytes": "every logit row read once + the sampled position's rows re-read "
+                         "(2 rows at a rejection, 1 for a bonus; accepted_len of this batch)",
+                "ms_per_launch": ms_per_step}
+    cpu, parity = (None, None)
     if not args.no_cpu_baseline:
-        cpu = cpu_baseline(w)
-    cfg = synth.WORKLOADS[args.workload]
+        cpu, parity = cpu_baseline(w, seed, gpu_out)
+    if rotate:
+        l2_label = (f"{len(copies)} rotating input copies, {p1_all / 1e6:.2f} MB read per step: "
+                    f"{(len(copies) - 1) * p1_all / 1e6:.0f} MB touched between two uses of a copy "
+                    f"(>= 2 x the {l2 / 1e6:.0f} MB L2)")
+    else:
+        l2_label = (f"{p1_all / 1e6:.3f} MB read per step: each call timed alone (events around "
+                    f"it) after writing a {2 * l2 / 1e6:.0f} MB buffer (2 x L2)")
     line = {
         "metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
-        "config": {"workload": f"{args.workload} B={B} K={K} V={V} {w.dtype} logits",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": f"{name} B={B} K={K} V={V} {w.dtype} logits",
                    "B": B, "K": K, "V": V, "logits": w.dtype,
                    "T": describe_temperatures(w.temperature),
                    "k_per_row": ("ragged: K_b uniform in 0..%d, mean %.2f" % (K, float(w.k_per_row.mean()))
                                  if ragged else f"every row {K}"),
-                   "l2": f"{len(copies)} rotating input copies of {w.logit_bytes() / 1e6:.2f} MB "
-                         f"(each larger than the 129 MB L2)",
+                   "l2": l2_label,
                    "parallelism": f"{world} independent replicas, own batch per GPU"},
         "roofline": roofline,
-        "step_roofline": {"achieved": step_gbs, "frac": step_gbs / hbm, "unit": "GB/s",
-                          "bytes_per_step": p1_bytes + p2_bytes,
-                          "accept_sample_ms_per_launch": k2_ms, "accept_sample_bytes": p2_bytes},
+        "parity": parity,
         "cpu_baseline": cpu,
         "e2e": {"value": positions / (e2e_ms * 1e-3), "unit": "positions/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": gpu_launches,
         "clocks": clocks,
         "extra": {"rows_per_s": B * world / (ms_per_step * 1e-3),
+                  "gb_per_s": step_gbs,
+                  "frac_of_nominal_8tbs": step_gbs / 8000.0,
+                  "pass1_bytes": p1_bytes, "resample_bytes": p2_bytes,
                   "plug_us_per_call": plug_us,
                   "verify_and_plug_us_per_step": fused_us,
                   "emitted_tokens_per_step": int((accepted + 1).sum()),
                   "mean_accepted_len": float(accepted.mean()),
-                  "peak_nominal_gbs": 8000.0, "frac_of_nominal": step_gbs / 8000.0},
+                  "device_flags": dev_flags},
     }
-    print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    del copies, host
+    return line
 
 
 def describe_temperatures(T):
@@ -514,7 +577,7 @@ def describe_temperatures(T):
     return body + (f", {greedy} greedy rows" if greedy else "")
 
 
-def stored_traffic(workload, kernel="sv_row_stats_kernel"):
+def stored_traffic(workload, kernel="sv_fused_kernel"):
     """DRAM bytes per launch of ``kernel`` from the committed ncu summary of
     this workload, or None when the summary was taken on other kernel
     sources (or is missing)."""
@@ -538,10 +601,11 @@ def stored_traffic(workload, kernel="sv_row_stats_kernel"):
 # the sources each kernel is built from (a stored ncu figure applies while
 # they are unchanged)
 KERNEL_SOURCES = {
+    "sv_fused_kernel": ("sv_common.cuh", "sv_stream.cuh", "sv_plug.cuh", "sv_sample.cuh",
+                        "sv_fused.cuh", "exp2_table.inc"),
     "sv_row_stats_kernel": ("sv_common.cuh", "sv_stream.cuh"),
-    "sv_row_stats_compact_kernel": ("sv_common.cuh", "sv_stream.cuh"),
-    "sv_accept_sample_kernel": ("sv_common.cuh", "sv_stream.cuh", "sv_plug.cuh", "sv_sample.cuh",
-                                "exp2_table.inc"),
+    "sv_tree_kernel": ("sv_common.cuh", "sv_stream.cuh", "sv_plug.cuh", "sv_sample.cuh",
+                       "sv_tree.cuh"),
 }
 
 
@@ -554,7 +618,7 @@ def code_only(text: str) -> str:
     return " ".join(text.split())
 
 
-def kernel_rev(kernel="sv_row_stats_kernel"):
+def kernel_rev(kernel="sv_fused_kernel"):
     """Hash of one kernel's sources (code only, see code_only)."""
     import hashlib
     h = hashlib.sha1()
@@ -677,7 +741,7 @@ def run_tree(args):
     line = {
         "metric": METRIC, "value": positions / (ms_per_step * 1e-3), "unit": "positions/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
         "config": {"workload": f"{args.workload} B={B} N={Nn} nodes V={V} {w.dtype} logits",
                    "B": B, "N": Nn, "V": V, "logits": w.dtype, "T": "0 (greedy tree)",
@@ -735,9 +799,11 @@ def cpu_baseline_tree(w, budget_s=12.0, sample_rows=4):
 def main():
     args = parse()
     from speculative_decoding_verification_25_gb300 import synth
-    tree = bool(synth.WORKLOADS[args.workload].get("tree"))
+    tree = args.workload != "all" and bool(synth.WORKLOADS[args.workload].get("tree"))
     if args.impl == "reference":
-        run_reference(args)
+        for name in (FIVE if args.workload == "all" else (args.workload,)):
+            args.workload = name
+            run_reference(args)
     elif tree:
         run_tree(args)
     else:

@@ -36,10 +36,8 @@
  *   - kernels are launched as programmatic dependents of the preceding
  *     kernel on the stream, so they may be scheduled while it drains.  Each
  *     waits (griddepcontrol.wait) for that kernel to complete before its
- *     first memory access, except the acceptance/sampling launch of the
- *     combined calls: it directly follows the same call's streaming launch
- *     and reads only caller inputs before its wait.  Stream order is kept
- *     for every read and write the caller can observe;
+ *     first memory access, so stream order is kept for every read and write
+ *     the caller can observe;
  *   - host-detectable errors return a status before anything is launched;
  *     row-level problems found on the device never fault or trap: the row is
  *     written as an error row (accepted_len = -1, all out_tokens -1) and a
@@ -82,13 +80,15 @@ extern "C" {
 #define SV_DEV_PLUG_CLIPPED 16u    /* spec_verify_plug: a row's tokens did not all fit */
 #define SV_DEV_BAD_LENGTH 32u      /* spec_verify_plug: seq_len[b] outside [0, max_len] */
 #define SV_DEV_BAD_TREE 64u        /* spec_verify_tree: a parent or node token out of range */
+#define SV_DEV_TIMEOUT 128u        /* a wait inside the verify kernel gave up (see spec_verify) */
 
 #define SV_MAX_K 16
 #define SV_MAX_TREE_NODES 128
 
 /*
  * Bytes of scratch the caller must pass to spec_verify for this shape.
- * Pure host arithmetic; returns 0 for invalid arguments.
+ * Pure host arithmetic; returns 0 for invalid arguments.  The workspace
+ * must be zero-filled before its first use (see spec_verify).
  */
 size_t spec_verify_workspace_bytes(int B, int K, int V, int dtype);
 
@@ -114,16 +114,28 @@ int spec_verify_max_vocab(int dtype);
  *                  greedy and error rows.
  *   logq_out       optional [B, K] float32 out: log q_t(x_t), same layout.
  *   workspace      device scratch, 16-byte aligned, at least
- *                  spec_verify_workspace_bytes(B, K, V, dtype) bytes; its
- *                  contents need no initialisation and are overwritten.
+ *                  spec_verify_workspace_bytes(B, K, V, dtype) bytes, ALL
+ *                  ZERO before its first use (e.g. cudaMemsetAsync once
+ *                  after allocation).  It holds the kernel's counters,
+ *                  tickets and per-row slots; every call returns all of it
+ *                  to zero except the 4-byte device flag word at offset 0,
+ *                  which then holds that call's SV_DEV_* flags.  A zeroed
+ *                  workspace may therefore serve calls of any shape in turn.
  *   stream         cudaStream_t to enqueue on.
  *
  * B == 0 is a no-op (pointers may then be NULL).  Returns SV_OK or an
  * SV_ERR_* code; on an error code nothing has been launched.  Two calls
  * that share a workspace must be ordered on the device (same stream).
  *
- * Enqueues the two launches of spec_verify_row_stats and
- * spec_verify_accept_sample below.
+ * One launch: a persistent grid of (SM count x resident CTAs) whose warps
+ * stream every logit row once, fold each row's statistics, run the
+ * acceptance scan of each batch row as soon as its rows are complete, and
+ * then weigh the sampled position's rows tile by tile and locate the
+ * token.  Warps hand work to one another through the workspace; each wait
+ * is bounded, and a wait that gives up (only possible when the grid
+ * cannot be resident at once, e.g. on a GPU shared with other work) sets
+ * SV_DEV_TIMEOUT: that call's outputs are then unspecified and the
+ * workspace must be zero-filled again before its next use.
  */
 int spec_verify(const void* target_logits, const void* draft_logits, int dtype,
                 const int32_t* draft_tokens, const float* uniforms,
@@ -163,56 +175,6 @@ int spec_verify_ragged(const void* target_logits, const void* draft_logits, int 
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * The two stages spec_verify runs, for callers that schedule them apart
- * (or time them).  spec_verify_row_stats + spec_verify_accept_sample on the
- * same stream, inputs and workspace give exactly spec_verify's result.
- *
- * spec_verify_row_stats streams every target row and the draft rows of
- * rows with T > 0 once and leaves one partial per 2 KB tile in the
- * workspace: (tile max m, sum of e^((x - m)/T)) for the softmax
- * normaliser, or (max logit, its lowest index) for T == 0 rows.  It also
- * clears the device flag word.
- *
- * spec_verify_accept_sample folds those partials into per-position
- * statistics, runs the acceptance test and draws the replacement or bonus
- * token (re-reading only the logit rows of the one position that needs a
- * draw).  It must follow spec_verify_row_stats on the same stream (or be
- * ordered after it by an event).  Arguments and return codes are those of
- * spec_verify.
- */
-int spec_verify_row_stats(const void* target_logits, const void* draft_logits, int dtype,
-                          const float* temperature, int B, int K, int V,
-                          void* workspace, size_t workspace_bytes, void* stream);
-
-int spec_verify_accept_sample(const void* target_logits, const void* draft_logits, int dtype,
-                              const int32_t* draft_tokens, const float* uniforms,
-                              const float* temperature, int B, int K, int V,
-                              int32_t* accepted_len, int32_t* out_tokens,
-                              float* logp_out, float* logq_out,
-                              void* workspace, size_t workspace_bytes, void* stream);
-
-/*
- * The same two stages for adaptive verification (spec_verify_ragged's rule
- * and arguments; k_per_row as there).  spec_verify_ragged_row_stats streams
- * only the rows that the lengths select: target rows 0..K_b and, for T > 0,
- * draft rows 0..K_b-1.  spec_verify_ragged_accept_sample must be given the
- * same k_per_row.  Run back to back on one stream and workspace, they give
- * exactly spec_verify_ragged's result.
- */
-int spec_verify_ragged_row_stats(const void* target_logits, const void* draft_logits, int dtype,
-                                 const float* temperature, const int32_t* k_per_row,
-                                 int B, int K, int V,
-                                 void* workspace, size_t workspace_bytes, void* stream);
-
-int spec_verify_ragged_accept_sample(const void* target_logits, const void* draft_logits,
-                                     int dtype, const int32_t* draft_tokens,
-                                     const float* uniforms, const float* temperature,
-                                     const int32_t* k_per_row, int B, int K, int V,
-                                     int32_t* accepted_len, int32_t* out_tokens,
-                                     float* logp_out, float* logq_out,
-                                     void* workspace, size_t workspace_bytes, void* stream);
-
-/*
  * Reads the device-side row flags (SV_DEV_*) that the last spec_verify call
  * on this workspace OR-ed in.  Enqueues a 4-byte copy on `stream` and
  * SYNCHRONISES that stream; `flags` is a HOST pointer.  Returns SV_OK,
@@ -240,9 +202,9 @@ int spec_verify_device_errors(const void* workspace, void* stream, uint32_t* fla
  * (256-byte aligned) in this library.  Shapes whose
  * spec_verify_workspace_bytes(B, K, V, dtype) exceeds that size are
  * rejected with SV_ERR_TOO_LARGE before anything touches the device (at
- * V = 128256 bf16 and K = 4 that admits B up to 924).  Nothing in the
- * scratch must start at zero: the streaming launch resets its flag word and
- * writes every partial before the accept launch reads it.
+ * V = 128256 bf16 and K = 4 that admits B up to 1278).  The array starts
+ * zero-filled with the module and every call leaves it so, as spec_verify
+ * requires of a workspace.
  *
  * Setup: the first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) and keeps it; a failed lookup returns
@@ -330,10 +292,10 @@ int spec_verify_plug(const int32_t* accepted_len, const int32_t* out_tokens, int
                      uint32_t* flags, void* stream);
 
 /*
- * spec_verify (or spec_verify_ragged) with the plug step fused into the
- * acceptance/sampling launch: one call, two launches, no third launch for
- * the plug.  The thread block that writes a row's last token also appends
- * the row's emitted tokens to `tokens` and advances `seq_len`, with exactly
+ * spec_verify (or spec_verify_ragged) with the plug step fused into its
+ * launch: one call, one launch, no second launch for the plug.  The warp
+ * that writes a row's last token also appends the row's emitted tokens to
+ * `tokens` and advances `seq_len`, with exactly
  * spec_verify_plug's rule: same arguments (tokens, seq_len, max_len,
  * last_token), same results.  Its SV_DEV_PLUG_CLIPPED / SV_DEV_BAD_LENGTH
  * flags go to the workspace word with the call's other device flags (read

@@ -30,6 +30,7 @@ SV_DEV_BAD_K = 8
 SV_DEV_PLUG_CLIPPED = 16
 SV_DEV_BAD_LENGTH = 32
 SV_DEV_BAD_TREE = 64
+SV_DEV_TIMEOUT = 128
 
 SV_MAX_K = 16
 SV_MAX_TREE_NODES = 128
@@ -43,9 +44,6 @@ _SIG = {
     "spec_verify_max_vocab": (_I, [_I]),
     "spec_verify": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P,
                          ctypes.c_size_t, _P]),
-    "spec_verify_row_stats": (_I, [_P, _P, _I, _P, _I, _I, _I, _P, ctypes.c_size_t, _P]),
-    "spec_verify_accept_sample": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P,
-                                       ctypes.c_size_t, _P]),
     "spec_verify_device_errors": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
     "spec_verify_static": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "spec_verify_tree_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
@@ -53,10 +51,6 @@ _SIG = {
     "spec_verify_plug": (_I, [_P, _P, _I, _I, _P, _P, _I, _P, _P, _P]),
     "spec_verify_ragged": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P,
                                 ctypes.c_size_t, _P]),
-    "spec_verify_ragged_row_stats": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _P, ctypes.c_size_t,
-                                          _P]),
-    "spec_verify_ragged_accept_sample": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P,
-                                              _P, _P, ctypes.c_size_t, _P]),
     "spec_verify_and_plug": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                                   _I, _P, _P, ctypes.c_size_t, _P]),
     "spec_verify_status_string": (ctypes.c_char_p, [_I]),
@@ -112,22 +106,6 @@ def spec_verify_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr, temp
                                   stream_handle))
 
 
-def spec_verify_row_stats_raw(target_ptr, draft_ptr, dtype, temperature_ptr, B, K, V,
-                              workspace_ptr, workspace_bytes, stream_handle) -> int:
-    return int(load().spec_verify_row_stats(target_ptr, draft_ptr, dtype, temperature_ptr, B, K, V,
-                                            workspace_ptr, workspace_bytes, stream_handle))
-
-
-def spec_verify_accept_sample_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr,
-                                  temperature_ptr, B, K, V, accepted_ptr, out_tokens_ptr,
-                                  logp_ptr, logq_ptr, workspace_ptr, workspace_bytes,
-                                  stream_handle) -> int:
-    return int(load().spec_verify_accept_sample(target_ptr, draft_ptr, dtype, tokens_ptr,
-                                                uniforms_ptr, temperature_ptr, B, K, V,
-                                                accepted_ptr, out_tokens_ptr, logp_ptr, logq_ptr,
-                                                workspace_ptr, workspace_bytes, stream_handle))
-
-
 def spec_verify_ragged_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr,
                            temperature_ptr, k_per_row_ptr, B, K, V, accepted_ptr, out_tokens_ptr,
                            logp_ptr, logq_ptr, workspace_ptr, workspace_bytes, stream_handle) -> int:
@@ -136,23 +114,6 @@ def spec_verify_ragged_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_pt
                                          temperature_ptr, k_per_row_ptr, B, K, V, accepted_ptr,
                                          out_tokens_ptr, logp_ptr, logq_ptr, workspace_ptr,
                                          workspace_bytes, stream_handle))
-
-
-def spec_verify_ragged_row_stats_raw(target_ptr, draft_ptr, dtype, temperature_ptr, k_per_row_ptr,
-                                     B, K, V, workspace_ptr, workspace_bytes, stream_handle) -> int:
-    return int(load().spec_verify_ragged_row_stats(target_ptr, draft_ptr, dtype, temperature_ptr,
-                                                   k_per_row_ptr, B, K, V, workspace_ptr,
-                                                   workspace_bytes, stream_handle))
-
-
-def spec_verify_ragged_accept_sample_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr,
-                                         temperature_ptr, k_per_row_ptr, B, K, V, accepted_ptr,
-                                         out_tokens_ptr, logp_ptr, logq_ptr, workspace_ptr,
-                                         workspace_bytes, stream_handle) -> int:
-    return int(load().spec_verify_ragged_accept_sample(
-        target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr, temperature_ptr, k_per_row_ptr,
-        B, K, V, accepted_ptr, out_tokens_ptr, logp_ptr, logq_ptr, workspace_ptr, workspace_bytes,
-        stream_handle))
 
 
 def spec_verify_and_plug_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr,

@@ -77,31 +77,29 @@ def run_oracle(w, rows=None, workers=None):
                               sum((p.mode for p in parts), []))
 
 
-def run_gpu_stages(w, device="cuda:0", want_logprobs=True):
-    """The same step through the two-launch entry points
-    (spec_verify_row_stats, then spec_verify_accept_sample)."""
-    import torch
-    from speculative_decoding_verification_25_gb300 import _native as N
-    d = device_tensors(w, device)
-    dt = N.SV_BF16 if w.dtype == "bf16" else N.SV_F32
-    B, K, V = w.B, w.K, w.V
-    nbytes = N.spec_verify_workspace_bytes(B, K, V, dt)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
-    acc = torch.empty(B, dtype=torch.int32, device=device)
-    out = torch.empty(B, K + 1, dtype=torch.int32, device=device)
-    lp = torch.empty(B, K, dtype=torch.float32, device=device) if want_logprobs else None
-    lq = torch.empty(B, K, dtype=torch.float32, device=device) if want_logprobs else None
-    sh = torch.cuda.current_stream().cuda_stream
-    st = N.spec_verify_row_stats_raw(d["target"].data_ptr(), d["draft"].data_ptr(), dt,
-                                     d["temperature"].data_ptr(), B, K, V, ws.data_ptr(), nbytes, sh)
-    assert st == N.SV_OK, st
-    st = N.spec_verify_accept_sample_raw(
-        d["target"].data_ptr(), d["draft"].data_ptr(), dt, d["draft_tokens"].data_ptr(),
-        d["uniforms"].data_ptr(), d["temperature"].data_ptr(), B, K, V, acc.data_ptr(),
-        out.data_ptr(), lp.data_ptr() if lp is not None else None,
-        lq.data_ptr() if lq is not None else None, ws.data_ptr(), nbytes, sh)
-    assert st == N.SV_OK, st
-    torch.cuda.synchronize()
-    return dict(accepted=acc.cpu().numpy(), out_tokens=out.cpu().numpy(),
-                logp=lp.cpu().numpy() if lp is not None else None,
-                logq=lq.cpu().numpy() if lq is not None else None)
+def _workload_oracle_job(args):
+    name, seed, rows = args
+    from oracle import oracle
+    from speculative_decoding_verification_25_gb300 import synth
+    w = synth.make(name, seed=seed, rows=rows)
+    kpr = getattr(w, "k_per_row", None)
+    if kpr is not None:
+        return oracle.spec_verify_ragged(w.target, w.draft, w.draft_tokens, w.uniforms,
+                                         w.temperature, kpr, dtype=w.dtype)
+    return oracle.spec_verify(w.target, w.draft, w.draft_tokens, w.uniforms, w.temperature,
+                              dtype=w.dtype)
+
+
+def run_oracle_workload(name, seed, B, workers=None):
+    """The oracle on every row of a named synthetic workload.  Each worker
+    rebuilds its own rows from the seed (the generator draws every row from
+    streams of its own), so no logits cross process boundaries."""
+    from oracle import oracle
+    workers = workers or max(1, min(16, os.cpu_count() or 1))
+    chunks = [c for c in np.array_split(np.arange(B), min(workers * 4, B)) if len(c)]
+    with mp.get_context("spawn").Pool(min(workers, len(chunks))) as pool:
+        parts = pool.map(_workload_oracle_job, [(name, seed, c) for c in chunks])
+    cat = lambda f: np.concatenate([getattr(p, f) for p in parts])
+    return oracle.BatchResult(cat("accepted_len"), cat("out_tokens"), cat("logp"), cat("logq"),
+                              cat("ratio_margin"), cat("cdf_margin"),
+                              sum((p.mode for p in parts), []))

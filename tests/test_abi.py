@@ -44,14 +44,28 @@ def test_every_declared_symbol_is_exported(N):
     assert set(_declared_functions()) <= set(N._SIG)
 
 
+def _layout_bytes(B, K, V, elt, chunk_tiles=4):
+    """The workspace layout the header describes: a 256-byte header, then
+    256-byte aligned regions -- a chunk ticket per row, a scan ticket, a
+    sampling ticket and a ready flag per batch row, 32 bytes of draw
+    parameters per batch row, two 64-bit statistics words per row, one
+    64-bit partial per chunk of chunk_tiles 2 KB tiles per row, and a
+    32-byte record per tile of every batch row's sampled row."""
+    al = lambda x: (x + 255) // 256 * 256
+    rows = B * (2 * K + 1)
+    tpr = -(-V // (2048 // elt))
+    cpr = -(-tpr // chunk_tiles)
+    off = 256
+    for size in (rows * 4, B * 4, B * 4, B * 4, B * 32, rows * 16, rows * cpr * 8, B * tpr * 32):
+        off = al(off + size)
+    return off
+
+
 def test_workspace_bytes_arithmetic(N):
-    # a 256-byte header, then one 8-byte partial per 2 KB tile of every target and draft row
-    B, K, V = 64, 4, 128256
-    tiles = -(-V // 1024)
-    assert N.spec_verify_workspace_bytes(B, K, V, N.SV_BF16) == 256 + (B * (K + 1) + B * K) * tiles * 8
-    tiles32 = -(-V // 512)
-    assert N.spec_verify_workspace_bytes(B, K, V, N.SV_F32) == 256 + (B * (K + 1) + B * K) * tiles32 * 8
-    assert N.spec_verify_workspace_bytes(0, 4, 1000, N.SV_F32) == 256
+    for B, K, V in ((64, 4, 128256), (1, 4, 1000), (512, 10, 262144), (3, 16, 33), (256, 8, 152064)):
+        assert N.spec_verify_workspace_bytes(B, K, V, N.SV_BF16) == _layout_bytes(B, K, V, 2)
+        assert N.spec_verify_workspace_bytes(B, K, V, N.SV_F32) == _layout_bytes(B, K, V, 4)
+    assert N.spec_verify_workspace_bytes(0, 4, 1000, N.SV_F32) == _layout_bytes(0, 4, 1000, 4)
     for bad in ((-1, 4, 10, 0), (1, 0, 10, 0), (1, 17, 10, 0), (1, 4, 0, 0), (1, 4, 10, 2),
                 (1, 4, N.spec_verify_max_vocab(0) + 1, 0)):
         assert N.spec_verify_workspace_bytes(*bad) == 0
@@ -120,7 +134,7 @@ def test_static_entry_point_rejects_before_touching_the_device(N):
             if N.spec_verify_workspace_bytes(B, 4, 128256, N.SV_BF16) <= N.SV_STATIC_SCRATCH_BYTES]
     assert fits and fits == list(range(1, fits[-1] + 1)) and fits[-1] >= 64
     assert call(B=fits[-1] + 1, V=128256) == N.SV_ERR_TOO_LARGE
-    assert call(B=256, K=8, V=152064, dtype=N.SV_F32) == N.SV_ERR_TOO_LARGE
+    assert call(B=512, K=10, V=262144) == N.SV_ERR_TOO_LARGE
     assert "static" in N.status_string(N.SV_ERR_TOO_LARGE)
 
 
@@ -147,24 +161,6 @@ def test_ragged_entry_point_checks_its_length_array(N):
     assert call(None, B=0) == N.SV_OK
     assert N.spec_verify_ragged_raw(FAKE, FAKE, 9, FAKE, FAKE, FAKE, FAKE, 2, 4, 1024, FAKE, FAKE,
                                     None, None, FAKE, 1 << 30, None) == N.SV_ERR_DTYPE
-
-
-def test_ragged_stage_entry_points_check_their_length_array(N):
-    def rs(kpr, B=2, dt=None):
-        return N.spec_verify_ragged_row_stats_raw(FAKE, FAKE, N.SV_BF16 if dt is None else dt, FAKE,
-                                                  kpr, B, 4, 1024, FAKE, 1 << 30, None)
-
-    def acc(kpr, B=2):
-        return N.spec_verify_ragged_accept_sample_raw(FAKE, FAKE, N.SV_BF16, FAKE, FAKE, FAKE, kpr,
-                                                      B, 4, 1024, FAKE, FAKE, None, None, FAKE,
-                                                      1 << 30, None)
-    for call in (rs, acc):
-        assert call(None) == N.SV_ERR_NULL
-        assert call(FAKE + 2) == N.SV_ERR_ALIGN
-        assert call(None, B=0) == N.SV_OK
-    assert rs(FAKE, dt=9) == N.SV_ERR_DTYPE
-    assert N.spec_verify_ragged_row_stats_raw(FAKE, FAKE, N.SV_BF16, FAKE, FAKE, 2, 4, 1024, FAKE,
-                                              16, None) == N.SV_ERR_WORKSPACE
 
 
 def test_fused_plug_entry_point_checks_arguments(N):

@@ -41,7 +41,7 @@ def test_verify_and_plug_replay_in_a_cuda_graph(name):
     B, K, V = w.B, w.K, w.V
     static = {k: v.clone() for k, v in inputs[0].items()}
     nb = N.spec_verify_workspace_bytes(B, K, V, N.SV_BF16)
-    workspace = torch.empty(nb, dtype=torch.uint8, device="cuda:0")
+    workspace = torch.zeros(nb, dtype=torch.uint8, device="cuda:0")
     out = api.VerifyResult(torch.empty(B, dtype=torch.int32, device="cuda:0"),
                            torch.empty(B, K + 1, dtype=torch.int32, device="cuda:0"))
     tokens = torch.full((B, MAX_LEN), -1, dtype=torch.int32, device="cuda:0")

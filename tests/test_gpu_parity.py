@@ -9,7 +9,7 @@ import pytest
 from speculative_decoding_verification_25_gb300 import synth
 
 from _parity import check_structure, compare
-from gpu_util import device_tensors, run_gpu, run_gpu_stages, run_oracle
+from gpu_util import device_tensors, run_gpu, run_oracle, run_oracle_workload
 
 pytestmark = pytest.mark.gpu
 
@@ -73,69 +73,59 @@ def test_llama3_stochastic_full_size():
     _assert_parity(total, int(0.001 * total.rows))
 
 
-def test_long_draft_mixed_t_full_size():
-    """B=256, K=8, V=152064 fp32: every greedy row and 48 tempered rows vs the oracle,
-    structure on all rows."""
-    w = synth.make("long_draft_mixed_t", seed=0, workers=synth.default_workers())
+@pytest.mark.parametrize("seed", [0, 1])
+def test_long_draft_mixed_t_full_size(seed):
+    """B=256, K=8, V=152064 fp32 (26 greedy rows, T ~ U(0.3, 1.5) on the
+    others): every row against the oracle."""
+    w = synth.make("long_draft_mixed_t", seed=seed, workers=synth.default_workers())
     g = run_gpu(w)
     assert not check_structure(g["accepted"], g["out_tokens"], w.draft_tokens, w.V)
-    greedy = np.nonzero(w.temperature == 0)[0]
-    temp = np.nonzero(w.temperature != 0)[0]
-    rows = np.concatenate([greedy, temp[np.linspace(0, len(temp) - 1, 48).astype(int)]])
-    sub = synth.make("long_draft_mixed_t", seed=0, rows=rows, workers=synth.default_workers())
-    ref = run_oracle(sub)
-    rep = compare(ref, g["accepted"], g["out_tokens"], g["logp"], g["logq"], w.temperature, rows=rows)
-    print("long_draft_mixed_t parity:", rep)
-    assert rep.greedy_rows == len(greedy) == 26
+    temperature = w.temperature
+    del w
+    ref = run_oracle_workload("long_draft_mixed_t", seed, 256)
+    rep = compare(ref, g["accepted"], g["out_tokens"], g["logp"], g["logq"], temperature)
+    print(f"long_draft_mixed_t seed {seed} parity:", rep)
+    assert rep.rows == 256 and rep.greedy_rows == 26 and rep.stochastic_rows == 230
     _assert_parity(rep, 0)
 
 
-def test_large_vocab_stress_full_size():
-    """B=512, K=10, V=262144 bf16 (5.6 GB of logits): all 256 greedy rows and 32
-    tempered rows vs the oracle, structure on all rows."""
-    w = synth.make("large_vocab_stress", seed=0, workers=synth.default_workers())
+@pytest.mark.parametrize("seed", [0, 1])
+def test_large_vocab_stress_full_size(seed):
+    """B=512, K=10, V=262144 bf16 (5.6 GB of logits; odd rows greedy, even
+    rows T = 0.7): every row against the oracle."""
+    w = synth.make("large_vocab_stress", seed=seed, workers=synth.default_workers())
     g = run_gpu(w)
     assert not check_structure(g["accepted"], g["out_tokens"], w.draft_tokens, w.V)
-    greedy = np.arange(1, 512, 2)
-    temp = np.arange(0, 512, 16)
-    rows = np.concatenate([greedy, temp])
-    ref = run_oracle(synth.make("large_vocab_stress", seed=0, rows=rows,
-                                workers=synth.default_workers()))
-    rep = compare(ref, g["accepted"], g["out_tokens"], g["logp"], g["logq"], w.temperature, rows=rows)
-    print("large_vocab_stress parity:", rep)
-    assert rep.greedy_rows == 256
-    _assert_parity(rep, 0)
-
-
-# ---------------------------------------------------------------- the two-launch entry points
-
-@pytest.mark.parametrize("name,seed", [("tiny_stochastic", 3), ("tiny_greedy", 3),
-                                       ("greedy_batch", 0), ("llama3_stochastic", 1)])
-def test_two_launch_stages_match_oracle(name, seed):
-    w = synth.make(name, seed=seed, workers=synth.default_workers())
-    g = run_gpu_stages(w)
-    ref = run_oracle(w)
-    assert not check_structure(g["accepted"], g["out_tokens"], w.draft_tokens, w.V)
-    rep = compare(ref, g["accepted"], g["out_tokens"], g["logp"], g["logq"], w.temperature)
+    temperature = w.temperature
+    del w
+    ref = run_oracle_workload("large_vocab_stress", seed, 512)
+    rep = compare(ref, g["accepted"], g["out_tokens"], g["logp"], g["logq"], temperature)
+    print(f"large_vocab_stress seed {seed} parity:", rep)
+    assert rep.rows == 512 and rep.greedy_rows == 256 and rep.stochastic_rows == 256
     _assert_parity(rep, 0)
 
 
 def test_shapes_change_on_one_workspace():
-    """Calls of different shapes share one (never initialised) workspace."""
+    """Calls of different shapes share one zero-filled workspace, and every
+    call leaves it zeroed again apart from the device flag word."""
     import torch
     from speculative_decoding_verification_25_gb300 import api
-    ws = torch.full((64 << 20,), 0xAB, dtype=torch.uint8, device="cuda:0")   # garbage
+    ws = torch.zeros((64 << 20,), dtype=torch.uint8, device="cuda:0")
     for name, rows in (("greedy_batch", range(7)), ("llama3_stochastic", range(12)),
-                       ("tiny_stochastic", None), ("llama3_stochastic", range(3))):
+                       ("tiny_stochastic", None), ("long_draft_mixed_t", range(5)),
+                       ("llama3_stochastic", range(3)), ("llama3_ragged", range(9))):
         w = synth.make(name, seed=2, rows=rows)
         d = device_tensors(w)
         r = api.spec_verify(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
-                            d["temperature"], want_logprobs=True, workspace=ws)
+                            d["temperature"], k_per_row=d.get("k_per_row"), want_logprobs=True,
+                            workspace=ws)
         torch.cuda.synchronize()
         ref = run_oracle(w, workers=1)
         rep = compare(ref, r.accepted_len.cpu().numpy(), r.out_tokens.cpu().numpy(),
                       r.logp.cpu().numpy(), r.logq.cpu().numpy(), w.temperature)
         _assert_parity(rep, 0)
+        nz = torch.nonzero(ws[4:]).flatten()
+        assert nz.numel() == 0, (name, (nz[:8] + 4).tolist())
 
 
 # ---------------------------------------------------------------- small shapes and edges
@@ -179,11 +169,12 @@ CASES = [
     (7, 4, 1000, "f32", 0), (6, 5, 4099, "bf16", 0), (5, 2, 8191, "f32", 0),
     (9, 3, 8192, "bf16", 0), (3, 6, 20000, "bf16", 1), (3, 4, 17001, "f32", 3),
     (2, 2, 65536, "bf16", 0), (2, 3, 70001, "f32", 0),
-    # V > 131072 bf16: clusters of 16 up to 32 rows, of 8 above
+    # rows of many tiles: chunks of 4 tiles with a ragged last chunk and tile
     (32, 2, 140000, "bf16", 0), (33, 2, 140000, "bf16", 0),
-    # small batches: the cluster doubles while B * 2c <= 152 SMs (>= 64 groups per CTA)
     (4, 4, 128256, "bf16", 0), (9, 3, 100000, "bf16", 0), (10, 3, 100000, "bf16", 0),
     (1, 4, 32000, "bf16", 0), (16, 2, 32000, "bf16", 0), (3, 4, 9000, "f32", 5),
+    # exactly one chunk per row, and one tile more
+    (5, 3, 4096, "bf16", 0), (5, 3, 4097, "bf16", 0), (5, 3, 2048, "f32", 0),
 ]
 
 

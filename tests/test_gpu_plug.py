@@ -102,7 +102,7 @@ def test_fused_plug_equals_verify_then_plug(name, rows):
     flags = torch.zeros(1, dtype=torch.int32, device="cuda:0")
     api.plug(ref, t_ref, L_ref, last_token=last_ref, flags=flags)
 
-    ws = torch.empty(N.spec_verify_workspace_bytes(B, K, w.V, N.SV_BF16 if w.dtype == "bf16"
+    ws = torch.zeros(N.spec_verify_workspace_bytes(B, K, w.V, N.SV_BF16 if w.dtype == "bf16"
                                                    else N.SV_F32), dtype=torch.uint8,
                      device="cuda:0")
     t_f, L_f = torch.from_numpy(tok0).cuda(), torch.from_numpy(L0).cuda()

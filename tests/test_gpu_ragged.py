@@ -98,9 +98,9 @@ def test_bad_lengths_are_error_rows_with_a_flag():
 
 
 @pytest.mark.parametrize("B,dtype", [(2048, "f32"), (2049, "bf16")])
-def test_batch_at_and_past_the_compact_limit(B, dtype):
-    # up to 2048 batch rows the streaming pass splits only the rows read;
-    # past that every warp takes a fixed share of all rows
+def test_large_ragged_batches(B, dtype):
+    # thousands of short rows: many batch rows per chunk window, most
+    # chunks one tile, rows of every length
     rng = np.random.default_rng(B)
     K, V = 3, 600
     w = _random(rng, B, K, V, dtype, rng.integers(0, K + 1, B))
@@ -111,8 +111,8 @@ def test_batch_at_and_past_the_compact_limit(B, dtype):
 
 
 def test_greedy_rows_without_lengths_skip_their_draft_rows():
-    # without verified lengths every warp takes a fixed share of all rows and
-    # skips the draft rows of greedy rows inside it
+    # the chunks of a greedy row's draft rows are skipped by the warps they
+    # fall to
     rng = np.random.default_rng(11)
     w = _random(rng, 40, 5, 5000, "bf16", np.full(40, 5))
     w = dataclasses.replace(w, k_per_row=None)
@@ -120,33 +120,3 @@ def test_greedy_rows_without_lengths_skip_their_draft_rows():
     g = run_gpu(w)
     ref = run_oracle(w)
     _assert_parity(compare(ref, g["accepted"], g["out_tokens"], g["logp"], g["logq"], w.temperature))
-
-
-def test_ragged_stages_equal_the_one_call_bit_for_bit():
-    import torch
-    from speculative_decoding_verification_25_gb300 import _native as N
-    w = synth.make("llama3_ragged", seed=1, rows=range(24))
-    one = run_gpu(w)
-    d = device_tensors(w)
-    dt = N.SV_BF16
-    B, K, V = w.B, w.K, w.V
-    nb = N.spec_verify_workspace_bytes(B, K, V, dt)
-    ws = torch.empty(nb, dtype=torch.uint8, device="cuda:0")
-    acc = torch.empty(B, dtype=torch.int32, device="cuda:0")
-    out = torch.empty(B, K + 1, dtype=torch.int32, device="cuda:0")
-    lp = torch.empty(B, K, dtype=torch.float32, device="cuda:0")
-    lq = torch.empty(B, K, dtype=torch.float32, device="cuda:0")
-    sh = torch.cuda.current_stream().cuda_stream
-    assert N.spec_verify_ragged_row_stats_raw(
-        d["target"].data_ptr(), d["draft"].data_ptr(), dt, d["temperature"].data_ptr(),
-        d["k_per_row"].data_ptr(), B, K, V, ws.data_ptr(), nb, sh) == N.SV_OK
-    assert N.spec_verify_ragged_accept_sample_raw(
-        d["target"].data_ptr(), d["draft"].data_ptr(), dt, d["draft_tokens"].data_ptr(),
-        d["uniforms"].data_ptr(), d["temperature"].data_ptr(), d["k_per_row"].data_ptr(), B, K, V,
-        acc.data_ptr(), out.data_ptr(), lp.data_ptr(), lq.data_ptr(), ws.data_ptr(), nb,
-        sh) == N.SV_OK
-    torch.cuda.synchronize()
-    np.testing.assert_array_equal(acc.cpu().numpy(), one["accepted"])
-    np.testing.assert_array_equal(out.cpu().numpy(), one["out_tokens"])
-    np.testing.assert_array_equal(lp.cpu().numpy().view(np.uint32), one["logp"].view(np.uint32))
-    np.testing.assert_array_equal(lq.cpu().numpy().view(np.uint32), one["logq"].view(np.uint32))

@@ -40,7 +40,7 @@ def test_static_scratch_matches_spec_verify_twice_in_a_row(name, rows):
 
     # the existing entry point on a caller workspace
     nbytes = N.spec_verify_workspace_bytes(B, K, V, dt)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda:0")
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda:0")
     ref = _outputs(B, K, "cuda:0")
     st = N.spec_verify_raw(ptrs[0], ptrs[1], dt, *ins, B, K, V, *[t.data_ptr() for t in ref],
                            ws.data_ptr(), nbytes, stream)
@@ -66,6 +66,19 @@ def test_static_scratch_matches_spec_verify_twice_in_a_row(name, rows):
         np.testing.assert_allclose(lp[sampled], lp_r[sampled], rtol=0, atol=1e-5)
         np.testing.assert_allclose(lq[sampled], lq_r[sampled], rtol=0, atol=1e-5)
         assert np.isnan(lp[~sampled]).all() and np.isnan(lq[~sampled]).all()
+
+    # and the calls allocate nothing: the device's free memory is the same
+    # before and after a run of them (outputs allocated beforehand)
+    outs = _outputs(B, K, "cuda:0")
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(20):
+        st = N.spec_verify_static_raw(ptrs[0], ptrs[1], dt, *ins, B, K, V,
+                                      *[t.data_ptr() for t in outs], stream)
+        assert st == N.SV_OK, N.status_string(st)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    np.testing.assert_array_equal(_host(outs)[1], tok_r)
 
 
 def test_static_scratch_rejects_a_shape_beyond_its_size():
