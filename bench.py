@@ -1,9 +1,10 @@
 """Benchmark of the batched verify-and-accept step (one JSON line on rank 0).
 
-A step is one spec_verify call -- one launch of the persistent kernel that
-streams every logit row, folds the statistics, runs the acceptance scan and
-draws the replacement or bonus token -- over one batch of the B=64, K=4,
-V=128256 bf16 workload (Zipf-like logits, T = 1), inputs resident in HBM.
+A step is one spec_verify call -- the streaming launch that reads every
+logit row once, then the draw launch that folds the statistics, runs the
+acceptance scan and draws the replacement or bonus token -- over one batch
+of the B=64, K=4, V=128256 bf16 workload (Zipf-like logits, T = 1), inputs
+resident in HBM.
 Input copies rotate so that every step reads data L2 has evicted (each
 copy's logits, 147.75 MB, exceed the 129 MB L2); a workload too small for
 that is timed one call at a time with an L2 flush before each.
@@ -409,7 +410,7 @@ def bench_workload(args, name, rank, world, local):
         barrier()
         t_ms = sum(a.elapsed_time(e) for a, e in evs)
     t_ms = max_over_ranks(t_ms, world)
-    gpu_launches = args.steps
+    gpu_launches = 2 * args.steps
     accepted = acc.cpu().numpy()
     if args.profile:
         sampler.stop()
@@ -514,9 +515,10 @@ def bench_workload(args, name, rank, world, local):
     p1_bytes, p2_bytes = algorithmic_bytes(w, accepted)
     hbm, peak_src = peaks()
     step_gbs = (p1_bytes + p2_bytes) / (ms_per_step * 1e-3) / 1e9
+    t1, t2 = stored_traffic(name, "sv_row_stats_kernel"), stored_traffic(name, "sv_draw_kernel")
     roofline = {"bound": "hbm", "achieved": step_gbs, "peak": hbm, "unit": "GB/s",
-                "frac": step_gbs / hbm, "traffic": stored_traffic(name, "sv_fused_kernel"),
-                "kernel": "sv_fused_kernel (the whole step is this one launch)",
+                "frac": step_gbs / hbm, "traffic": t1 + t2 if t1 and t2 else None,
+                "kernel": "the whole step: sv_row_stats_kernel + sv_draw_kernel, back to back",
                 "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_src == "measured" else "fallback",
                 "bytes_per_launch": p1_bytes + p2_bytes,
@@ -577,7 +579,7 @@ def describe_temperatures(T):
     return body + (f", {greedy} greedy rows" if greedy else "")
 
 
-def stored_traffic(workload, kernel="sv_fused_kernel"):
+def stored_traffic(workload, kernel="sv_row_stats_kernel"):
     """DRAM bytes per launch of ``kernel`` from the committed ncu summary of
     this workload, or None when the summary was taken on other kernel
     sources (or is missing)."""
@@ -601,9 +603,10 @@ def stored_traffic(workload, kernel="sv_fused_kernel"):
 # the sources each kernel is built from (a stored ncu figure applies while
 # they are unchanged)
 KERNEL_SOURCES = {
-    "sv_fused_kernel": ("sv_common.cuh", "sv_stream.cuh", "sv_plug.cuh", "sv_sample.cuh",
-                        "sv_fused.cuh", "exp2_table.inc"),
     "sv_row_stats_kernel": ("sv_common.cuh", "sv_stream.cuh"),
+    "sv_row_stats_compact_kernel": ("sv_common.cuh", "sv_stream.cuh"),
+    "sv_draw_kernel": ("sv_common.cuh", "sv_stream.cuh", "sv_plug.cuh", "sv_sample.cuh",
+                       "sv_draw.cuh", "exp2_table.inc"),
     "sv_tree_kernel": ("sv_common.cuh", "sv_stream.cuh", "sv_plug.cuh", "sv_sample.cuh",
                        "sv_tree.cuh"),
 }
@@ -618,7 +621,7 @@ def code_only(text: str) -> str:
     return " ".join(text.split())
 
 
-def kernel_rev(kernel="sv_fused_kernel"):
+def kernel_rev(kernel="sv_row_stats_kernel"):
     """Hash of one kernel's sources (code only, see code_only)."""
     import hashlib
     h = hashlib.sha1()

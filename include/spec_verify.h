@@ -80,15 +80,16 @@ extern "C" {
 #define SV_DEV_PLUG_CLIPPED 16u    /* spec_verify_plug: a row's tokens did not all fit */
 #define SV_DEV_BAD_LENGTH 32u      /* spec_verify_plug: seq_len[b] outside [0, max_len] */
 #define SV_DEV_BAD_TREE 64u        /* spec_verify_tree: a parent or node token out of range */
-#define SV_DEV_TIMEOUT 128u        /* a wait inside the verify kernel gave up (see spec_verify) */
+#define SV_DEV_OUT_OF_BOUNDS 256u  /* checked build only (libspec_verify_checked.so, compiled with
+                                      -DSV_CHECKED): an index failed its bounds test and the
+                                      access was skipped */
 
 #define SV_MAX_K 16
 #define SV_MAX_TREE_NODES 128
 
 /*
  * Bytes of scratch the caller must pass to spec_verify for this shape.
- * Pure host arithmetic; returns 0 for invalid arguments.  The workspace
- * must be zero-filled before its first use (see spec_verify).
+ * Pure host arithmetic; returns 0 for invalid arguments.
  */
 size_t spec_verify_workspace_bytes(int B, int K, int V, int dtype);
 
@@ -114,28 +115,23 @@ int spec_verify_max_vocab(int dtype);
  *                  greedy and error rows.
  *   logq_out       optional [B, K] float32 out: log q_t(x_t), same layout.
  *   workspace      device scratch, 16-byte aligned, at least
- *                  spec_verify_workspace_bytes(B, K, V, dtype) bytes, ALL
- *                  ZERO before its first use (e.g. cudaMemsetAsync once
- *                  after allocation).  It holds the kernel's counters,
- *                  tickets and per-row slots; every call returns all of it
- *                  to zero except the 4-byte device flag word at offset 0,
- *                  which then holds that call's SV_DEV_* flags.  A zeroed
- *                  workspace may therefore serve calls of any shape in turn.
+ *                  spec_verify_workspace_bytes(B, K, V, dtype) bytes; its
+ *                  contents need no initialisation and are overwritten (the
+ *                  4-byte word at offset 0 then holds the call's SV_DEV_*
+ *                  flags).
  *   stream         cudaStream_t to enqueue on.
  *
  * B == 0 is a no-op (pointers may then be NULL).  Returns SV_OK or an
  * SV_ERR_* code; on an error code nothing has been launched.  Two calls
  * that share a workspace must be ordered on the device (same stream).
  *
- * One launch: a persistent grid of (SM count x resident CTAs) whose warps
- * stream every logit row once, fold each row's statistics, run the
- * acceptance scan of each batch row as soon as its rows are complete, and
- * then weigh the sampled position's rows tile by tile and locate the
- * token.  Warps hand work to one another through the workspace; each wait
- * is bounded, and a wait that gives up (only possible when the grid
- * cannot be resident at once, e.g. on a GPU shared with other work) sets
- * SV_DEV_TIMEOUT: that call's outputs are then unspecified and the
- * workspace must be zero-filled again before its next use.
+ * Two launches: a persistent grid of (SM count x resident CTAs) whose warps
+ * stream every logit row once and leave one partial per 2 KB tile, then G
+ * CTAs per batch row that fold the row's statistics, run the acceptance
+ * scan, weigh the sampled position's rows tile by tile and locate the
+ * token.  No kernel waits on another's flags: the second launch waits for
+ * the first (griddepcontrol.wait) and its CTAs meet through one atomic
+ * ticket per row.
  */
 int spec_verify(const void* target_logits, const void* draft_logits, int dtype,
                 const int32_t* draft_tokens, const float* uniforms,
@@ -202,9 +198,9 @@ int spec_verify_device_errors(const void* workspace, void* stream, uint32_t* fla
  * (256-byte aligned) in this library.  Shapes whose
  * spec_verify_workspace_bytes(B, K, V, dtype) exceeds that size are
  * rejected with SV_ERR_TOO_LARGE before anything touches the device (at
- * V = 128256 bf16 and K = 4 that admits B up to 1278).  The array starts
- * zero-filled with the module and every call leaves it so, as spec_verify
- * requires of a workspace.
+ * V = 128256 bf16 and K = 4 that admits B up to 593).  Nothing in the
+ * scratch must start at zero: the streaming launch resets its flag word and
+ * tickets and writes every partial before the draw launch reads it.
  *
  * Setup: the first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) and keeps it; a failed lookup returns

@@ -10,6 +10,8 @@ import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libspec_verify.so")
+# the same library compiled with index checks (tests only)
+LIB_CHECKED_PATH = os.path.join(PKG, "libspec_verify_checked.so")
 
 SV_F32 = 0
 SV_BF16 = 1
@@ -30,7 +32,7 @@ SV_DEV_BAD_K = 8
 SV_DEV_PLUG_CLIPPED = 16
 SV_DEV_BAD_LENGTH = 32
 SV_DEV_BAD_TREE = 64
-SV_DEV_TIMEOUT = 128
+SV_DEV_OUT_OF_BOUNDS = 256
 
 SV_MAX_K = 16
 SV_MAX_TREE_NODES = 128
@@ -57,6 +59,7 @@ _SIG = {
 }
 
 _lib = None
+_lib_checked = None
 
 
 class SpecVerifyError(RuntimeError):
@@ -72,13 +75,28 @@ def load() -> ctypes.CDLL:
         if not os.path.exists(LIB_PATH):
             raise ImportError(
                 f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
-        lib = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in _SIG.items():
-            fn = getattr(lib, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = lib
+        _lib = _open(LIB_PATH)
     return _lib
+
+
+def _open(path: str) -> ctypes.CDLL:
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIG.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+def load_checked() -> ctypes.CDLL:
+    """The checked build (every kernel index tested against its buffer; a
+    failure sets SV_DEV_OUT_OF_BOUNDS), with the same C entry points."""
+    global _lib_checked
+    if _lib_checked is None:
+        if not os.path.exists(LIB_CHECKED_PATH):
+            raise ImportError(f"{LIB_CHECKED_PATH} is not built")
+        _lib_checked = _open(LIB_CHECKED_PATH)
+    return _lib_checked
 
 
 def spec_verify_workspace_bytes(B: int, K: int, V: int, dtype: int) -> int:

@@ -47,8 +47,7 @@ def workspace_for(B: int, K: int, V: int, dtype: int, device: torch.device,
                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """A cached device workspace large enough for this shape, one per
     (device, stream): calls on one stream run in order and may share it,
-    calls on different streams may overlap and must not.  It is zero-filled
-    when allocated, and every verify call leaves it zeroed again."""
+    calls on different streams may overlap and must not."""
     need = N.spec_verify_workspace_bytes(B, K, V, dtype)
     if need == 0:
         raise ValueError(f"invalid shape B={B} K={K} V={V}")
@@ -58,7 +57,7 @@ def workspace_for(B: int, K: int, V: int, dtype: int, device: torch.device,
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < need:
         with torch.cuda.stream(st):   # allocated for use on this stream
-            ws = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=device)
+            ws = torch.empty(max(need, 1 << 20), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
 

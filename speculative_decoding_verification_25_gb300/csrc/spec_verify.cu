@@ -2,12 +2,16 @@
 // geometry and the C ABI declared in include/spec_verify.h.
 //
 // spec_verify, spec_verify_ragged, spec_verify_and_plug and
-// spec_verify_static are one launch each: sv_fused_kernel, a persistent grid
-// (SM count x resident CTAs) that streams every logit row once, folds the
-// rows' statistics, runs the acceptance scan and draws the replacement or
-// bonus token (sv_fused.cuh).  spec_verify_tree runs the streaming kernel of
-// sv_stream.cuh over the target slots and then sv_tree_kernel;
-// spec_verify_plug is one small launch of its own.
+// spec_verify_static are two launches each on the caller's stream:
+//   1. sv_row_stats_kernel (sv_stream.cuh), a persistent grid (SM count x
+//      resident CTAs) whose warps stream contiguous ranges of 2 KB row
+//      tiles and leave one partial per tile; with verified lengths per row
+//      (B <= kCompactMaxB) its compact instantiation, whose warps split only
+//      the rows read;
+//   2. sv_draw_kernel (sv_draw.cuh), G CTAs per batch row: statistics fold,
+//      acceptance scan, and the draw over the sampled position's tiles.
+// spec_verify_tree runs the first kernel over the target slots and then
+// sv_tree_kernel; spec_verify_plug is one small launch of its own.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -15,20 +19,20 @@
 #include <mutex>
 
 #include "spec_verify.h"
-#include "sv_fused.cuh"
+#include "sv_draw.cuh"
 #include "sv_plug.cuh"
 #include "sv_tree.cuh"
 
 namespace {
 
-constexpr size_t kHeaderBytes = 256;   // grid control words; device flags at offset 0
+constexpr size_t kHeaderBytes = 256;   // device flag word at offset 0
 constexpr int kMaxDevices = 64;
 
 struct DeviceCache {
   std::once_flag once;
   int sm_count = 0;
-  int fused_blocks_per_sm[2][2][2] = {};      // [dtype][aligned][plug]
-  int row_stats_blocks_per_sm[2][2] = {};     // [dtype][aligned]
+  int row_stats_blocks_per_sm[2][2][2] = {};  // [dtype][aligned][compact]
+  int draw_blocks_per_sm = 1;
   cudaError_t init_error = cudaSuccess;
   // device address of g_static_scratch, looked up by the first
   // spec_verify_static call on this device
@@ -39,8 +43,7 @@ struct DeviceCache {
 
 DeviceCache g_devices[kMaxDevices];
 
-// Scratch of spec_verify_static: one array per device, loaded with the
-// module (zero-filled, as every verify workspace must start).
+// Scratch of spec_verify_static: one array per device, loaded with the module.
 __device__ __align__(256) unsigned char g_static_scratch[SV_STATIC_SCRATCH_BYTES];
 
 int vec_of(int dtype) { return dtype == SV_BF16 ? 8 : 4; }
@@ -57,27 +60,33 @@ long long tiles_per_row(int V, int dtype) {
   return (V + tile_elems - 1) / tile_elems;
 }
 
-long long chunks_per_row(long long tpr) { return (tpr + sv::kChunkTiles - 1) / sv::kChunkTiles; }
-
 template <typename E, bool kAligned>
-void* fused_fn(bool plug) {
-  return plug ? (void*)sv::sv_fused_kernel<E, kAligned, true>
-              : (void*)sv::sv_fused_kernel<E, kAligned, false>;
+void* row_stats_fn(bool compact) {
+  return compact ? (void*)sv::sv_row_stats_compact_kernel<E, kAligned>
+                 : (void*)sv::sv_row_stats_kernel<E, kAligned>;
 }
-void* pick_fused(int dtype, bool aligned, bool plug) {
+// compact: the kernel that splits only the rows read (verified lengths given,
+// B <= kCompactMaxB)
+void* pick_row_stats(int dtype, bool aligned, bool compact) {
   if (dtype == SV_BF16)
-    return aligned ? fused_fn<sv::Bf16, true>(plug) : fused_fn<sv::Bf16, false>(plug);
-  return aligned ? fused_fn<sv::F32, true>(plug) : fused_fn<sv::F32, false>(plug);
+    return aligned ? row_stats_fn<sv::Bf16, true>(compact) : row_stats_fn<sv::Bf16, false>(compact);
+  return aligned ? row_stats_fn<sv::F32, true>(compact) : row_stats_fn<sv::F32, false>(compact);
 }
-void* pick_row_stats(int dtype, bool aligned) {
+bool use_compact(const int32_t* k_per_row, int B) {
+  return k_per_row != nullptr && B <= sv::kCompactMaxB;
+}
+template <typename E, bool kAligned>
+void* draw_fn(bool plug) {
+  return plug ? (void*)sv::sv_draw_kernel<E, kAligned, true>
+              : (void*)sv::sv_draw_kernel<E, kAligned, false>;
+}
+void* pick_draw(int dtype, bool aligned, bool plug) {
   if (dtype == SV_BF16)
-    return aligned ? (void*)sv::sv_row_stats_kernel<sv::Bf16, true>
-                   : (void*)sv::sv_row_stats_kernel<sv::Bf16, false>;
-  return aligned ? (void*)sv::sv_row_stats_kernel<sv::F32, true>
-                 : (void*)sv::sv_row_stats_kernel<sv::F32, false>;
+    return aligned ? draw_fn<sv::Bf16, true>(plug) : draw_fn<sv::Bf16, false>(plug);
+  return aligned ? draw_fn<sv::F32, true>(plug) : draw_fn<sv::F32, false>(plug);
 }
 
-// SM count and occupancy of the persistent kernels; once per device.
+// SM count and occupancy of the kernels; once per device.
 DeviceCache* device_cache(int dev) {
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
   DeviceCache& dc = g_devices[dev];
@@ -85,19 +94,19 @@ DeviceCache* device_cache(int dev) {
     cudaError_t e = cudaDeviceGetAttribute(&dc.sm_count, cudaDevAttrMultiProcessorCount, dev);
     for (int dt = 0; dt < 2 && e == cudaSuccess; ++dt) {
       for (int al = 0; al < 2 && e == cudaSuccess; ++al) {
-        for (int pl = 0; pl < 2 && e == cudaSuccess; ++pl) {
+        for (int cp = 0; cp < 2 && e == cudaSuccess; ++cp) {
           int nb = 0;
-          e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, pick_fused(dt, al != 0, pl != 0),
-                                                            sv::kFThreads, 0);
-          dc.fused_blocks_per_sm[dt][al][pl] = nb > 0 ? nb : 1;
-        }
-        int nb = 0;
-        if (e == cudaSuccess)
-          e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, pick_row_stats(dt, al != 0),
+          e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, pick_row_stats(dt, al != 0, cp != 0),
                                                             sv::kP1Threads, 0);
-        dc.row_stats_blocks_per_sm[dt][al] = nb > 0 ? nb : 1;
+          dc.row_stats_blocks_per_sm[dt][al][cp] = nb > 0 ? nb : 1;
+        }
       }
     }
+    int nb = 0;
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, pick_draw(SV_BF16, true, false),
+                                                        sv::kDThreads, 0);
+    dc.draw_blocks_per_sm = nb > 0 ? nb : 1;
     dc.init_error = e;
   });
   return &dc;
@@ -108,37 +117,40 @@ bool aligned_to(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace of the verify calls, in 256-byte aligned regions after the
-// header: per stacked row a chunk ticket, per batch row a scan ticket, a
-// sampling ticket and a ready flag, per batch row the published draw
-// parameters, per stacked row its statistics (two 64-bit words), per
-// stacked row one 64-bit partial per chunk, per batch row one 32-byte record
-// per tile of the sampled row.  All of it is zero between calls.
+// header (device flag word at offset 0): one float2 partial per 2 KB tile of
+// every target and draft row; a draw ticket per batch row; per batch row 32
+// part records and one record per tile of the sampled row (32 bytes each).
+// The streaming launch clears the flag word and the tickets and writes every
+// partial the draw launch reads, so nothing needs initialising.
 struct Layout {
-  size_t fold_ticket, scan_ticket, samp_ticket, ready, rowstate, rowstat, partials, recs, total;
+  size_t partials, tickets, part_recs, tile_recs, total;
 };
 Layout layout(int B, int K, int V, int dtype) {
   const long long rows = (long long)B * (2 * K + 1);
   const long long tpr = tiles_per_row(V, dtype);
   Layout L;
   size_t off = kHeaderBytes;
-  L.fold_ticket = off;
-  off = align_up(off + (size_t)rows * 4, 256);
-  L.scan_ticket = off;
-  off = align_up(off + (size_t)B * 4, 256);
-  L.samp_ticket = off;
-  off = align_up(off + (size_t)B * 4, 256);
-  L.ready = off;
-  off = align_up(off + (size_t)B * 4, 256);
-  L.rowstate = off;
-  off = align_up(off + (size_t)B * sizeof(sv::RowState), 256);
-  L.rowstat = off;
-  off = align_up(off + (size_t)rows * 16, 256);
   L.partials = off;
-  off = align_up(off + (size_t)(rows * chunks_per_row(tpr)) * 8, 256);
-  L.recs = off;
+  off = align_up(off + (size_t)(rows * tpr) * sizeof(float2), 256);
+  L.tickets = off;
+  off = align_up(off + (size_t)B * 4, 256);
+  L.part_recs = off;
+  off = align_up(off + (size_t)B * sv::kMaxParts * 32, 256);
+  L.tile_recs = off;
   off = align_up(off + (size_t)((long long)B * tpr) * 32, 256);
   L.total = off;
   return L;
+}
+
+// CTAs per batch row for the draw launch: enough to fill the GPU once, and
+// at least one per 64 tiles of a row (more waves for large batches), at most
+// kMaxParts and one per tile.
+int draw_parts(int B, long long tpr, const DeviceCache* dc) {
+  const long long fill = (long long)dc->sm_count * dc->draw_blocks_per_sm / (B > 0 ? B : 1);
+  long long g = fill > (tpr + 63) / 64 ? fill : (tpr + 63) / 64;
+  if (g > sv::kMaxParts) g = sv::kMaxParts;
+  if (g > tpr) g = tpr;
+  return g < 1 ? 1 : (int)g;
 }
 
 }  // namespace
@@ -204,18 +216,63 @@ struct PlugTarget {
   int max_len = 0;
 };
 
-// The whole step: one launch of the persistent kernel.
+// The streaming launch (partials of every row read, flag word and draw
+// tickets cleared); tickets == nullptr for the tree's use.
+int launch_row_stats(const void* target_logits, const void* draft_logits, int dtype,
+                     const float* temperature, const int32_t* k_per_row, int B, int K, int V,
+                     void* workspace, unsigned* tickets, DeviceCache* dc, cudaStream_t st) {
+  const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
+  const long long tpr = tiles_per_row(V, dtype);
+  const long long n_target_rows = (long long)B * (K + 1);
+  sv::RowStatsArgs ra;
+  memset(&ra, 0, sizeof(ra));
+  ra.target = target_logits;
+  ra.draft = draft_logits;
+  ra.temperature = temperature;
+  ra.B = B;
+  ra.K = K;
+  ra.V = V;
+  ra.tiles_per_row = (int)tpr;
+  ra.n_tiles = (n_target_rows + (long long)B * K) * tpr;
+  ra.n_target_rows = (int)n_target_rows;
+  ra.k_per_row = k_per_row;
+  ra.partials = (float2*)((char*)workspace + kHeaderBytes);
+  ra.err = (unsigned*)workspace;
+  ra.tickets = tickets;
+  ra.n_tickets = tickets ? B : 0;
+  // persistent grid: every SM filled once; every warp a contiguous tile range
+  const int warps_per_block = sv::kP1Threads / 32;
+  const bool compact = use_compact(k_per_row, B);
+  long long blocks =
+      (long long)dc->sm_count * dc->row_stats_blocks_per_sm[dtype][aligned ? 1 : 0][compact ? 1 : 0];
+  const long long need = (ra.n_tiles + warps_per_block - 1) / warps_per_block;
+  if (blocks > need) blocks = need;
+  if (blocks < 1) blocks = 1;
+  void* args[] = {&ra};
+  return launch_early(pick_row_stats(dtype, aligned, compact), dim3((unsigned)blocks),
+                      dim3(sv::kP1Threads), args, st) == cudaSuccess
+             ? SV_OK
+             : SV_ERR_CUDA;
+}
+
+// The whole step: the streaming launch, then the draw launch.  The draw
+// grid may start as the streaming kernel's CTAs exit (programmatic
+// dependent launch): it reads only caller inputs before it waits for the
+// partials.
 int launch_verify(const void* target_logits, const void* draft_logits, int dtype,
                   const int32_t* draft_tokens, const float* uniforms, const float* temperature,
                   const int32_t* k_per_row, int B, int K, int V, int32_t* accepted_len,
                   int32_t* out_tokens, float* logp_out, float* logq_out, void* workspace,
                   DeviceCache* dc, cudaStream_t st, const PlugTarget& plug = PlugTarget()) {
-  const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
   const Layout L = layout(B, K, V, dtype);
-  const long long tpr = tiles_per_row(V, dtype);
-  const long long cpr = chunks_per_row(tpr);
   char* ws = (char*)workspace;
-  sv::FusedArgs a;
+  unsigned* tickets = (unsigned*)(ws + L.tickets);
+  const int r = launch_row_stats(target_logits, draft_logits, dtype, temperature, k_per_row, B, K,
+                                 V, workspace, tickets, dc, st);
+  if (r != SV_OK) return r;
+  const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
+  const long long tpr = tiles_per_row(V, dtype);
+  sv::DrawArgs a;
   memset(&a, 0, sizeof(a));
   a.target = target_logits;
   a.draft = draft_logits;
@@ -227,19 +284,13 @@ int launch_verify(const void* target_logits, const void* draft_logits, int dtype
   a.K = K;
   a.V = V;
   a.tpr = (int)tpr;
-  a.cpr = (int)cpr;
   a.n_target_rows = B * (K + 1);
-  a.n_chunks = (long long)B * (2 * K + 1) * cpr;
-  a.n_items = (long long)B * tpr;
-  a.hdr = (sv::FusedHeader*)ws;
-  a.fold_ticket = (unsigned*)(ws + L.fold_ticket);
-  a.scan_ticket = (unsigned*)(ws + L.scan_ticket);
-  a.samp_ticket = (unsigned*)(ws + L.samp_ticket);
-  a.ready = (unsigned*)(ws + L.ready);
-  a.rowstate = (sv::RowState*)(ws + L.rowstate);
-  a.rowstat = (unsigned long long*)(ws + L.rowstat);
-  a.partials = (unsigned long long*)(ws + L.partials);
-  a.recs = (float4*)(ws + L.recs);
+  a.parts = draw_parts(B, tpr, dc);
+  a.partials = (const float2*)(ws + L.partials);
+  a.err = (unsigned*)ws;
+  a.tickets = tickets;
+  a.part_recs = (float4*)(ws + L.part_recs);
+  a.tile_recs = (float4*)(ws + L.tile_recs);
   a.accepted_len = accepted_len;
   a.out_tokens = out_tokens;
   a.logp_out = logp_out;
@@ -248,16 +299,10 @@ int launch_verify(const void* target_logits, const void* draft_logits, int dtype
   a.plug_seq_len = plug.seq_len;
   a.plug_last = plug.last_token;
   a.plug_max_len = plug.max_len;
-  // persistent grid: every SM filled once, no more warps than work items
-  const bool pl = plug.tokens != nullptr;
-  long long blocks = (long long)dc->sm_count * dc->fused_blocks_per_sm[dtype][aligned ? 1 : 0][pl ? 1 : 0];
-  const long long work = a.n_chunks > a.n_items ? a.n_chunks : a.n_items;
-  const long long need = (work + sv::kFWarps - 1) / sv::kFWarps;
-  if (blocks > need) blocks = need;
-  if (blocks < 1) blocks = 1;
   void* args[] = {&a};
-  return launch_early(pick_fused(dtype, aligned, pl), dim3((unsigned)blocks), dim3(sv::kFThreads),
-                      args, st) == cudaSuccess
+  const long long blocks = (long long)B * a.parts;
+  return launch_early(pick_draw(dtype, aligned, plug.tokens != nullptr), dim3((unsigned)blocks),
+                      dim3(sv::kDThreads), args, st) == cudaSuccess
              ? SV_OK
              : SV_ERR_CUDA;
 }
@@ -441,13 +486,13 @@ int spec_verify_tree(const void* target_logits, int dtype, const int32_t* node_t
   ra.k_per_row = nullptr;
   ra.partials = (float2*)((char*)workspace + tree_partials_offset());
   ra.err = (unsigned*)workspace;
-  long long blocks = (long long)dc->sm_count * dc->row_stats_blocks_per_sm[dtype][aligned ? 1 : 0];
+  long long blocks = (long long)dc->sm_count * dc->row_stats_blocks_per_sm[dtype][aligned ? 1 : 0][0];
   const long long need_blocks = (ra.n_tiles + sv::kP1Threads / 32 - 1) / (sv::kP1Threads / 32);
   if (blocks > need_blocks) blocks = need_blocks;
   if (blocks < 1) blocks = 1;
   void* args1[] = {&ra};
-  if (launch_early(pick_row_stats(dtype, aligned), dim3((unsigned)blocks), dim3(sv::kP1Threads),
-                   args1, st) != cudaSuccess)
+  if (launch_early(pick_row_stats(dtype, aligned, false), dim3((unsigned)blocks),
+                   dim3(sv::kP1Threads), args1, st) != cudaSuccess)
     return SV_ERR_CUDA;
   // 2. one CTA per tree
   sv::TreeArgs ta;

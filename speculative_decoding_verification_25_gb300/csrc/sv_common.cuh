@@ -14,6 +14,18 @@ namespace sv {
 #define SV_NEG_INF (-__int_as_float(0x7f800000))
 constexpr float kFltMin = 1.17549435e-38f;
 
+// The checked build (compiled with -DSV_CHECKED): every global index the
+// verify kernel forms is tested against its buffer's extent before the
+// access; a failed test skips the access and sets kDevOutOfBounds in the
+// device flags instead of faulting.  The plain build compiles the tests
+// away.
+#ifdef SV_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+constexpr unsigned kDevOutOfBounds = 256u;
+
 // ----------------------------------------------------------------- element types
 // A "vector" is 16 bytes of one logit row held as four 32-bit words:
 // 8 bf16 (two per word, element 2i in the low half) or 4 float32.
@@ -31,6 +43,10 @@ struct Bf16 {
     asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(h) : "l"((const unsigned short*)base + i));
     return __uint_as_float(((uint32_t)h) << 16);
   }
+  // a float32 value cut to a bf16 one (toward zero)
+  __device__ __forceinline__ static float round_logit(float v) {
+    return __uint_as_float(__float_as_uint(v) & 0xffff0000u);
+  }
 };
 
 struct F32 {
@@ -45,6 +61,7 @@ struct F32 {
     asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(f) : "l"((const float*)base + i));
     return f;
   }
+  __device__ __forceinline__ static float round_logit(float v) { return v; }
 };
 
 // 16-byte read-only streaming load that does not allocate in L1.
@@ -120,6 +137,14 @@ __device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
 // attribute returns from this at once.
 __device__ __forceinline__ void wait_for_preceding_grid() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next kernel on the stream (launched as a programmatic dependent)
+// be scheduled as this grid's CTAs exit, instead of after the last one: its
+// CTAs take the freed slots and run up to their own griddepcontrol.wait,
+// which still returns only once this grid has completed.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

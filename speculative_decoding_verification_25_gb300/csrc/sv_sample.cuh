@@ -15,8 +15,10 @@
 
 namespace sv {
 
-// A term whose probability exceeds this is evaluated in double-float
-// during sampling; smaller terms use the float32 path.
+// A term whose probability exceeds about this is evaluated in
+// double-float during sampling; smaller terms use the float32 path.  The
+// test is made on the logit itself (x >= a per-row threshold), so the
+// sweep and the locate step classify every element alike.
 constexpr float kBigProb = 1.0e-4f;
 
 // device flags (mirrors of the public SV_DEV_* values)
@@ -33,7 +35,7 @@ struct SampleCtx {
   float MCp, MCq;         // shifts (c-scaled) of the two rows
   float c_hi, c_lo;       // log2(e)/T as hi + lo
   float cw;               // c_used = S_p / S_q at the streaming pass's shifts
-  float thp, thq;         // big-term thresholds on 2^(x c - MC)
+  float tp, tq;           // large-term thresholds on the logits xp, xq
   DF L;                   // log2(e)/T as a double-float (= c_hi + c_lo)
 };
 
@@ -61,7 +63,7 @@ __device__ __forceinline__ void eval_pair(float xp, float xq, const SampleCtx& s
   const float ep = small_exp(xp, s.MCp, s);
   if (kResidual) {
     const float eq = small_exp(xq, s.MCq, s);
-    if (ep > s.thp || eq > s.thq) {
+    if (xp >= s.tp || xq >= s.tq) {
       const DF epd = big_exp(xp, s.MCp, s, tab);
       const DF eqd = big_exp(xq, s.MCq, s, tab);
       const DF d = df_sub(epd, df_mul_f(eqd, s.cw));
@@ -73,22 +75,22 @@ __device__ __forceinline__ void eval_pair(float xp, float xq, const SampleCtx& s
       q = DF{d > 0.f ? eq : 0.f, 0.f};
     }
   } else {
-    w = (ep > s.thp) ? big_exp(xp, s.MCp, s, tab) : DF{ep, 0.f};
+    w = (xp >= s.tp) ? big_exp(xp, s.MCp, s, tab) : DF{ep, 0.f};
     q = DF{0.f, 0.f};
   }
 }
 
-// Double-float weight of one large term at row position idx: w (and the
-// q that goes with a positive w), plus e^p and e^q for the row totals.
-template <typename E, bool kResidual>
-__device__ __forceinline__ void big_term(const SampleCtx& x, const float2* tab, long long idx, DF& w,
-                                         DF& q, DF& ep, DF& eq) {
-  ep = big_exp(E::load_scalar(x.rowP, idx), x.MCp, x, tab);
+// Double-float weight of one large term with logits xp (and xq): w (and
+// the q that goes with a positive w), plus e^p and e^q for the row totals.
+template <bool kResidual>
+__device__ __forceinline__ void big_term(const SampleCtx& x, const float2* tab, float xp, float xq,
+                                         DF& w, DF& q, DF& ep, DF& eq) {
+  ep = big_exp(xp, x.MCp, x, tab);
   w = ep;
   q = DF{0.f, 0.f};
   eq = DF{0.f, 0.f};
   if (kResidual) {
-    eq = big_exp(E::load_scalar(x.rowQ, idx), x.MCq, x, tab);
+    eq = big_exp(xq, x.MCq, x, tab);
     const DF d = df_sub(ep, df_mul_f(eq, x.cw));
     w = df_pos(d) ? d : DF{0.f, 0.f};
     q = df_pos(d) ? eq : DF{0.f, 0.f};

@@ -13,10 +13,16 @@
 //   only where its range leaves a row; the other tiles of that stretch get
 //   the neutral partial (-inf, 0).  Draft rows of greedy rows are not read.
 //
-//   The kernel may be launched before the preceding kernel on the stream
-//   has finished; it waits for it before its first memory access.  The
-//   greedy tree verification runs it over the target slots; its helpers
-//   (tile loads, the per-lane fold) also serve the verify step's kernel.
+//   With verified lengths per row (and B <= kCompactMaxB) many rows are not
+//   read, and which ones lives on the device.  sv_row_stats_compact_kernel
+//   then first counts, in every CTA, the rows read per segment (segment
+//   b < B: target rows of batch row b; segment B + b: its draft rows), and
+//   the warps split the tiles of those rows alone, in stacked order.
+//   Without lengths (sv_row_stats_kernel) every warp takes a fixed share of
+//   all tiles and skips the rows it need not read.
+//
+//   Both kernels may be launched before the preceding kernel on the stream
+//   has finished; they wait for it before their first memory access.
 //
 // The softmax normalisers are those of the rule's p_t = softmax(target / T)
 // and q_t = softmax(draft / T) in the lesson "Decodificação Especulativa e
@@ -32,6 +38,8 @@ constexpr int kMaxK = 16;
 constexpr int kTileVecsPerLane = 4;               // 4 x 16 B per lane
 constexpr int kTileVecs = 32 * kTileVecsPerLane;  // one 2 KB tile of one row
 constexpr int kP1Threads = 256;
+// batches up to this size split only the rows that are read (compact order)
+constexpr int kCompactMaxB = 2048;
 
 struct RowStatsArgs {
   const void* target;
@@ -44,7 +52,31 @@ struct RowStatsArgs {
   const int32_t* k_per_row;   // [B] drafted tokens each row verifies, or nullptr (all K)
   float2* partials;           // [n_target_rows + B*K][tiles_per_row]
   unsigned* err;
+  unsigned* tickets;          // [n_tickets] cleared for the draw launch that follows, or nullptr
+  int n_tickets;
 };
+
+// Clear the device flag word and the draw launch's tickets (block 0).  The
+// preceding kernel has completed (the caller waited for it), and the draw
+// launch that reads them runs after this grid.
+__device__ __forceinline__ void clear_control(const RowStatsArgs& a) {
+  if (blockIdx.x != 0) return;
+  if (threadIdx.x == 0) *a.err = 0u;
+  for (int i = threadIdx.x; i < a.n_tickets; i += blockDim.x) a.tickets[i] = 0u;
+}
+
+// Checked build: an index test guarding one access (always true, and
+// compiled away, in the plain build).
+__device__ __forceinline__ bool rs_in_bounds(const RowStatsArgs& a, bool ok) {
+  if (kChecked && !ok) {
+    atomicOr(a.err, kDevOutOfBounds);
+    return false;
+  }
+  return true;
+}
+__device__ __forceinline__ int rs_rows(const RowStatsArgs& a) {
+  return a.n_target_rows + (a.draft ? a.B * a.K : 0);
+}
 
 // float32 c = log2(e)/T, the same in both kernels
 __device__ __forceinline__ float log2e_over_f(float T) { return __fdiv_rn(kLog2eHi, T); }
@@ -256,7 +288,9 @@ struct Stretch {
 template <typename E, bool kAligned>
 __device__ __forceinline__ void load_at(uint32_t (&w)[kTileVecsPerLane][4], const WarpRows& wr,
                                         const TilePos& p, int lane, int full_end) {
-  load_tile<E, kAligned>(w, wr.rowp(p.row, E::kBytes), p.ti, lane, wr.a->V, p.ti < full_end, true);
+  const bool ok = rs_in_bounds(*wr.a, p.row >= 0 && p.row < rs_rows(*wr.a) && p.ti >= 0 &&
+                                          p.ti < wr.a->tiles_per_row);
+  load_tile<E, kAligned>(w, wr.rowp(p.row, E::kBytes), p.ti, lane, wr.a->V, p.ti < full_end, ok);
 }
 
 // Fold the tile at t (its data in w) into the open stretch; if the next tile
@@ -268,16 +302,174 @@ __device__ __forceinline__ void fold_at(const uint32_t (&w)[kTileVecsPerLane][4]
   fold_tile<E>(w, (long long)p.ti * kTileVecs + lane, sr.greedy, sr.c, sr.st);
   const bool more = np.t < wr.t1;
   if (!more || np.row != p.row) {
-    flush_stretch(wr.a->partials + (long long)p.row * wr.a->tiles_per_row, sr.first, p.ti, sr.greedy,
-                  lane, sr.st);
+    if (rs_in_bounds(*wr.a, p.row >= 0 && p.row < rs_rows(*wr.a) && sr.first >= 0 &&
+                                p.ti < wr.a->tiles_per_row))
+      flush_stretch(wr.a->partials + (long long)p.row * wr.a->tiles_per_row, sr.first, p.ti,
+                    sr.greedy, lane, sr.st);
     if (more) sr.open(wr, np.row, np.ti);
   }
+}
+
+// ------------------------------------------------------- compact order
+// Rows read in segment s: s < B target rows 0..K_b of batch row s; s >= B
+// draft rows 0..K_b-1 of batch row s - B (tempered rows only).  A batch row
+// with an invalid temperature or K_b outside [0, K] reads nothing.
+__device__ __forceinline__ int segment_rows(const RowStatsArgs& a, int s) {
+  const bool draft = s >= a.B;
+  const int b = draft ? s - a.B : s;
+  const float T = a.temperature ? __ldg(a.temperature + b) : 0.f;
+  const int kb = a.k_per_row ? __ldg(a.k_per_row + b) : a.K;
+  if (!valid_temperature(T) || kb < 0 || kb > a.K) return 0;
+  if (draft) return T == 0.f ? 0 : kb;
+  return kb + 1;
+}
+__device__ __forceinline__ int segment_row(const RowStatsArgs& a, int s, int r) {
+  return s < a.B ? s * (a.K + 1) + r : a.n_target_rows + (s - a.B) * a.K + r;
+}
+
+// pref[s] = rows read in segments before s, pref[2B] = all of them (every
+// thread of the CTA calls this)
+__device__ __forceinline__ void segment_prefix(const RowStatsArgs& a, int* pref, int* wsum) {
+  const int nseg = 2 * a.B;
+  const int per = (nseg + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int s0 = min((int)threadIdx.x * per, nseg), s1 = min(s0 + per, nseg);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int sum = 0;
+  for (int s = s0; s < s1; ++s) sum += segment_rows(a, s);
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int run = incl - sum;
+  for (int w = 0; w < warp; ++w) run += wsum[w];
+  for (int s = s0; s < s1; ++s) {
+    pref[s] = run;
+    run += segment_rows(a, s);
+  }
+  if (threadIdx.x == blockDim.x - 1) pref[nseg] = run;
+  __syncthreads();
+}
+
+// A position in a warp's range of the compact order: tile index t among the
+// tiles read, its segment, row within the segment, tile within the row.
+struct CompactPos {
+  long long t;
+  int seg, r, ti, row;
+  __device__ __forceinline__ CompactPos next(const RowStatsArgs& a, const int* pref) const {
+    CompactPos p = *this;
+    ++p.t;
+    if (++p.ti == a.tiles_per_row) {
+      p.ti = 0;
+      ++p.r;
+      const int nseg = 2 * a.B;
+      while (p.seg < nseg && p.r == pref[p.seg + 1] - pref[p.seg]) {
+        ++p.seg;
+        p.r = 0;
+      }
+      p.row = p.seg < nseg ? segment_row(a, p.seg, p.r) : -1;
+    }
+    return p;
+  }
+};
+
+__device__ __forceinline__ const char* stacked_rowp(const RowStatsArgs& a, int row, int elem_bytes) {
+  const bool d = row >= a.n_target_rows;
+  const long long r = d ? row - a.n_target_rows : row;
+  return (const char*)(d ? a.draft : a.target) + r * a.V * elem_bytes;
+}
+
+__device__ __forceinline__ void open_compact(const RowStatsArgs& a, const CompactPos& p, Stretch& sr) {
+  sr.row = p.row;
+  sr.first = p.ti;
+  const int b = p.seg < a.B ? p.seg : p.seg - a.B;
+  const float T = a.temperature ? __ldg(a.temperature + b) : 0.f;
+  sr.greedy = (T == 0.f);
+  sr.c = sr.greedy ? 0.f : log2e_over_f(T);
+  sr.st.reset();
+}
+
+template <typename E>
+__device__ __forceinline__ void fold_compact(const uint32_t (&w)[kTileVecsPerLane][4],
+                                             const RowStatsArgs& a, const CompactPos& p,
+                                             const CompactPos& np, long long t1, int lane,
+                                             Stretch& sr) {
+  fold_tile<E>(w, (long long)p.ti * kTileVecs + lane, sr.greedy, sr.c, sr.st);
+  const bool more = np.t < t1;
+  if (!more || np.row != p.row) {
+    if (rs_in_bounds(a, p.row >= 0 && p.row < rs_rows(a) && sr.first >= 0 && p.ti < a.tiles_per_row))
+      flush_stretch(a.partials + (long long)p.row * a.tiles_per_row, sr.first, p.ti, sr.greedy,
+                    lane, sr.st);
+    if (more) open_compact(a, np, sr);
+  }
+}
+
+// The tiles of one warp in the compact order (n_read rows are read).
+template <typename E, bool kAligned>
+__device__ __forceinline__ void stream_compact(const RowStatsArgs& a, const int* pref, int n_read, long long gw,
+                               long long nw, int lane, int full_end) {
+  const int tpr = a.tiles_per_row;
+  const long long total = (long long)n_read * tpr;
+  const long long t0 = gw * total / nw, t1 = (gw + 1) * total / nw;
+  if (t0 >= t1) return;
+  const int cr = (int)(t0 / tpr);
+  // the segment holding compact row cr: the last s with pref[s] <= cr
+  int lo = 0, hi = 2 * a.B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pref[mid] <= cr) lo = mid;
+    else hi = mid;
+  }
+  CompactPos pa;
+  pa.t = t0;
+  pa.seg = lo;
+  pa.r = cr - pref[lo];
+  pa.ti = (int)(t0 - (long long)cr * tpr);
+  pa.row = segment_row(a, pa.seg, pa.r);
+  uint32_t wa[kTileVecsPerLane][4], wb[kTileVecsPerLane][4];
+  load_tile<E, kAligned>(wa, stacked_rowp(a, pa.row, E::kBytes), pa.ti, lane, a.V, pa.ti < full_end,
+                         rs_in_bounds(a, pa.row >= 0 && pa.row < rs_rows(a) && pa.ti < a.tiles_per_row));
+  Stretch sr;
+  open_compact(a, pa, sr);
+  for (;;) {
+    const CompactPos pb = pa.next(a, pref);
+    if (pb.t < t1)
+      load_tile<E, kAligned>(wb, stacked_rowp(a, pb.row, E::kBytes), pb.ti, lane, a.V, pb.ti < full_end,
+                             rs_in_bounds(a, pb.row >= 0 && pb.row < rs_rows(a) && pb.ti < a.tiles_per_row));
+    fold_compact<E>(wa, a, pa, pb, t1, lane, sr);
+    if (pb.t >= t1) break;
+    pa = pb.next(a, pref);
+    if (pa.t < t1)
+      load_tile<E, kAligned>(wa, stacked_rowp(a, pa.row, E::kBytes), pa.ti, lane, a.V, pa.ti < full_end,
+                         rs_in_bounds(a, pa.row >= 0 && pa.row < rs_rows(a) && pa.ti < a.tiles_per_row));
+    fold_compact<E>(wb, a, pb, pa, t1, lane, sr);
+    if (pa.t >= t1) break;
+  }
+}
+
+template <typename E, bool kAligned>
+__global__ void __launch_bounds__(kP1Threads, 4) sv_row_stats_compact_kernel(RowStatsArgs a) {
+  wait_for_preceding_grid();   // before any access: the previous step may still read the workspace
+  allow_dependent_launch();
+  clear_control(a);
+  __shared__ int s_pref[2 * kCompactMaxB + 1];
+  __shared__ int s_wsum[kP1Threads / 32];
+  segment_prefix(a, s_pref, s_wsum);
+  const int tpr = a.tiles_per_row;
+  const int full_end = ((long long)tpr * kTileVecs * E::kVec == a.V) ? tpr : tpr - 1;
+  stream_compact<E, kAligned>(a, s_pref, s_pref[2 * a.B],
+                              ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5,
+                              ((long long)gridDim.x * blockDim.x) >> 5, threadIdx.x & 31, full_end);
 }
 
 template <typename E, bool kAligned>
 __global__ void __launch_bounds__(kP1Threads, 4) sv_row_stats_kernel(RowStatsArgs a) {
   wait_for_preceding_grid();   // before any access: the previous step may still read the workspace
-  if (blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0u;
+  allow_dependent_launch();
+  clear_control(a);
 
   const int lane = threadIdx.x & 31;
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;

@@ -28,7 +28,7 @@ struct TreeArgs {
   const int32_t* parents;        // [B, N]
   int B, N, V;
   int tiles_per_row;
-  const float2* partials;        // [B * (N+1)][tiles_per_row], zeroed once folded
+  const float2* partials;        // [B * (N+1)][tiles_per_row]
   unsigned* err;
   int32_t* accepted_len;         // [B]
   int32_t* out_tokens;           // [B, N+1]
@@ -70,9 +70,6 @@ __global__ void __launch_bounds__(kTreeThreads) sv_tree_kernel(TreeArgs a) {
       sm.mx[s] = st.x;
       sm.am[s] = __float_as_int(st.y);
     }
-    // leave the workspace zeroed, as the verify calls do
-    if (pp)
-      for (int i = hl; i < a.tiles_per_row; i += 16) const_cast<float2*>(pp)[i] = make_float2(0.f, 0.f);
   }
   __syncthreads();
   if (tid != 0) return;

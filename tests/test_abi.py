@@ -44,19 +44,16 @@ def test_every_declared_symbol_is_exported(N):
     assert set(_declared_functions()) <= set(N._SIG)
 
 
-def _layout_bytes(B, K, V, elt, chunk_tiles=4):
-    """The workspace layout the header describes: a 256-byte header, then
-    256-byte aligned regions -- a chunk ticket per row, a scan ticket, a
-    sampling ticket and a ready flag per batch row, 32 bytes of draw
-    parameters per batch row, two 64-bit statistics words per row, one
-    64-bit partial per chunk of chunk_tiles 2 KB tiles per row, and a
-    32-byte record per tile of every batch row's sampled row."""
+def _layout_bytes(B, K, V, elt):
+    """The workspace layout: a 256-byte header, then 256-byte aligned
+    regions -- one 8-byte partial per 2 KB tile of every target and draft
+    row, a 4-byte draw ticket per batch row, 32 part records and one record
+    per tile of the sampled row per batch row (32 bytes each)."""
     al = lambda x: (x + 255) // 256 * 256
     rows = B * (2 * K + 1)
     tpr = -(-V // (2048 // elt))
-    cpr = -(-tpr // chunk_tiles)
     off = 256
-    for size in (rows * 4, B * 4, B * 4, B * 4, B * 32, rows * 16, rows * cpr * 8, B * tpr * 32):
+    for size in (rows * tpr * 8, B * 4, B * 32 * 32, B * tpr * 32):
         off = al(off + size)
     return off
 

@@ -94,19 +94,20 @@ def test_stored_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     prof = tmp_path / "profiles"
     prof.mkdir()
     # the hash is taken over the real sources; only the summary file is fake
-    rev = bench.kernel_rev("sv_fused_kernel")
-    (prof / "sv_fused_kernel_w.md").write_text(
+    rev = bench.kernel_rev("sv_row_stats_kernel")
+    (prof / "sv_row_stats_kernel_w.md").write_text(
         f"# x\n\n- kernel_rev: {rev}\n- dram_bytes_per_launch: 12345\n")
-    (prof / "sv_fused_kernel_old.md").write_text(
+    (prof / "sv_row_stats_kernel_old.md").write_text(
         "- kernel_rev: 000000000000\n- dram_bytes_per_launch: 999\n")
     real_root = bench.ROOT
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "kernel_rev", lambda kernel="sv_fused_kernel": rev)
+    monkeypatch.setattr(bench, "kernel_rev", lambda kernel="sv_row_stats_kernel": rev)
     assert bench.stored_traffic("w") == 12345
     assert bench.stored_traffic("old") is None        # taken on other sources
     assert bench.stored_traffic("missing") is None
     monkeypatch.setattr(bench, "ROOT", real_root)
-    assert set(bench.KERNEL_SOURCES) == {"sv_fused_kernel", "sv_row_stats_kernel", "sv_tree_kernel"}
+    assert set(bench.KERNEL_SOURCES) == {"sv_row_stats_kernel", "sv_row_stats_compact_kernel",
+                                         "sv_draw_kernel", "sv_tree_kernel"}
     csrc = os.path.join(ROOT, "speculative_decoding_verification_25_gb300", "csrc")
     for files in bench.KERNEL_SOURCES.values():
         assert all(os.path.exists(os.path.join(csrc, f)) for f in files)

@@ -106,11 +106,10 @@ def test_large_vocab_stress_full_size(seed):
 
 
 def test_shapes_change_on_one_workspace():
-    """Calls of different shapes share one zero-filled workspace, and every
-    call leaves it zeroed again apart from the device flag word."""
+    """Calls of different shapes share one (never initialised) workspace."""
     import torch
     from speculative_decoding_verification_25_gb300 import api
-    ws = torch.zeros((64 << 20,), dtype=torch.uint8, device="cuda:0")
+    ws = torch.full((64 << 20,), 0xAB, dtype=torch.uint8, device="cuda:0")   # garbage
     for name, rows in (("greedy_batch", range(7)), ("llama3_stochastic", range(12)),
                        ("tiny_stochastic", None), ("long_draft_mixed_t", range(5)),
                        ("llama3_stochastic", range(3)), ("llama3_ragged", range(9))):
@@ -124,8 +123,6 @@ def test_shapes_change_on_one_workspace():
         rep = compare(ref, r.accepted_len.cpu().numpy(), r.out_tokens.cpu().numpy(),
                       r.logp.cpu().numpy(), r.logq.cpu().numpy(), w.temperature)
         _assert_parity(rep, 0)
-        nz = torch.nonzero(ws[4:]).flatten()
-        assert nz.numel() == 0, (name, (nz[:8] + 4).tolist())
 
 
 # ---------------------------------------------------------------- small shapes and edges

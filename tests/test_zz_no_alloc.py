@@ -40,7 +40,7 @@ def test_static_scratch_matches_spec_verify_twice_in_a_row(name, rows):
 
     # the existing entry point on a caller workspace
     nbytes = N.spec_verify_workspace_bytes(B, K, V, dt)
-    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda:0")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda:0")
     ref = _outputs(B, K, "cuda:0")
     st = N.spec_verify_raw(ptrs[0], ptrs[1], dt, *ins, B, K, V, *[t.data_ptr() for t in ref],
                            ws.data_ptr(), nbytes, stream)
