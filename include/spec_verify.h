@@ -198,7 +198,7 @@ int spec_verify_device_errors(const void* workspace, void* stream, uint32_t* fla
  * (256-byte aligned) in this library.  Shapes whose
  * spec_verify_workspace_bytes(B, K, V, dtype) exceeds that size are
  * rejected with SV_ERR_TOO_LARGE before anything touches the device (at
- * V = 128256 bf16 and K = 4 that admits B up to 593).  Nothing in the
+ * V = 128256 bf16 and K = 4 that admits B up to 637).  Nothing in the
  * scratch must start at zero: the streaming launch resets its flag word and
  * tickets and writes every partial before the draw launch reads it.
  *

@@ -118,12 +118,12 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace of the verify calls, in 256-byte aligned regions after the
 // header (device flag word at offset 0): one float2 partial per 2 KB tile of
-// every target and draft row; a draw ticket per batch row; per batch row 32
-// part records and one record per tile of the sampled row (32 bytes each).
-// The streaming launch clears the flag word and the tickets and writes every
-// partial the draw launch reads, so nothing needs initialising.
+// every target and draft row; a draw ticket per batch row; one 32-byte
+// record per tile of every batch row's sampled row.  The streaming launch
+// clears the flag word and the tickets and writes every partial the draw
+// launch reads, so nothing needs initialising.
 struct Layout {
-  size_t partials, tickets, part_recs, tile_recs, total;
+  size_t partials, counters, tile_recs, total;
 };
 Layout layout(int B, int K, int V, int dtype) {
   const long long rows = (long long)B * (2 * K + 1);
@@ -132,10 +132,8 @@ Layout layout(int B, int K, int V, int dtype) {
   size_t off = kHeaderBytes;
   L.partials = off;
   off = align_up(off + (size_t)(rows * tpr) * sizeof(float2), 256);
-  L.tickets = off;
+  L.counters = off;
   off = align_up(off + (size_t)B * 4, 256);
-  L.part_recs = off;
-  off = align_up(off + (size_t)B * sv::kMaxParts * 32, 256);
   L.tile_recs = off;
   off = align_up(off + (size_t)((long long)B * tpr) * 32, 256);
   L.total = off;
@@ -216,11 +214,11 @@ struct PlugTarget {
   int max_len = 0;
 };
 
-// The streaming launch (partials of every row read, flag word and draw
-// tickets cleared); tickets == nullptr for the tree's use.
+// The streaming launch (partials of every row read, flag word and the draw
+// launch's counters cleared); counters == nullptr for the tree's use.
 int launch_row_stats(const void* target_logits, const void* draft_logits, int dtype,
                      const float* temperature, const int32_t* k_per_row, int B, int K, int V,
-                     void* workspace, unsigned* tickets, DeviceCache* dc, cudaStream_t st) {
+                     void* workspace, unsigned* counters, DeviceCache* dc, cudaStream_t st) {
   const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
   const long long tpr = tiles_per_row(V, dtype);
   const long long n_target_rows = (long long)B * (K + 1);
@@ -238,8 +236,8 @@ int launch_row_stats(const void* target_logits, const void* draft_logits, int dt
   ra.k_per_row = k_per_row;
   ra.partials = (float2*)((char*)workspace + kHeaderBytes);
   ra.err = (unsigned*)workspace;
-  ra.tickets = tickets;
-  ra.n_tickets = tickets ? B : 0;
+  ra.tickets = counters;
+  ra.n_tickets = counters ? B : 0;
   // persistent grid: every SM filled once; every warp a contiguous tile range
   const int warps_per_block = sv::kP1Threads / 32;
   const bool compact = use_compact(k_per_row, B);
@@ -266,9 +264,9 @@ int launch_verify(const void* target_logits, const void* draft_logits, int dtype
                   DeviceCache* dc, cudaStream_t st, const PlugTarget& plug = PlugTarget()) {
   const Layout L = layout(B, K, V, dtype);
   char* ws = (char*)workspace;
-  unsigned* tickets = (unsigned*)(ws + L.tickets);
+  unsigned* counters = (unsigned*)(ws + L.counters);
   const int r = launch_row_stats(target_logits, draft_logits, dtype, temperature, k_per_row, B, K,
-                                 V, workspace, tickets, dc, st);
+                                 V, workspace, counters, dc, st);
   if (r != SV_OK) return r;
   const bool aligned = vector_path(target_logits, draft_logits, V, dtype);
   const long long tpr = tiles_per_row(V, dtype);
@@ -288,8 +286,7 @@ int launch_verify(const void* target_logits, const void* draft_logits, int dtype
   a.parts = draw_parts(B, tpr, dc);
   a.partials = (const float2*)(ws + L.partials);
   a.err = (unsigned*)ws;
-  a.tickets = tickets;
-  a.part_recs = (float4*)(ws + L.part_recs);
+  a.tickets = counters;
   a.tile_recs = (float4*)(ws + L.tile_recs);
   a.accepted_len = accepted_len;
   a.out_tokens = out_tokens;

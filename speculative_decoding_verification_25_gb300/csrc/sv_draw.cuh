@@ -16,14 +16,14 @@
 //   3. runs the left-to-right acceptance scan (one lane per position) --
 //      all G CTAs reach the same n, and part 0 writes the outputs;
 //   4. weighs its part of the sampled position's tiles -- w = max(p - q, 0)
-//      at a rejection, w = p for the bonus -- writing one record per tile
-//      (totals of w, of the e^q under positive w, of e^p and of e^q, as
-//      double-floats) and one record for the part;
+//      at a rejection, w = p for the bonus -- one warp per tile, writing
+//      one record per tile (totals of w, of the e^q under positive w, of
+//      e^p and of e^q, as double-floats);
 //   5. takes a ticket on the row; the CTA holding the last one locates the
-//      token: the part by the prefix of the part records, the tile by the
-//      prefix of that part's tile records, the element by a scan of that
-//      tile, re-read.
+//      token: the tile by a block-wide scan of the row's tile records, the
+//      element by a block-wide scan of that tile, re-read.
 // Greedy rows (T = 0) and error rows are finished by part 0 in step 3.
+// No CTA waits on another: the ticket is one atomic per CTA.
 //
 // Small terms are weighed in float32, terms whose probability exceeds
 // kBigProb in double-float; the exact c = S_p / S_q (from the double-float
@@ -57,8 +57,7 @@ struct DrawArgs {
   const float2* partials;     // [B*(K+1) + B*K][tpr] from the streaming pass
   unsigned* err;
   unsigned* tickets;          // [B], zero on entry (the streaming pass clears them)
-  float4* part_recs;          // [B][kMaxParts][2]: (W, Q), (Sp, Sq)
-  float4* tile_recs;          // [B][tpr][2]
+  float4* tile_recs;          // [B][tpr][2]: (W, Q), (P, S) as double-floats
   int32_t* accepted_len;
   int32_t* out_tokens;
   float* logp_out;
@@ -81,13 +80,15 @@ struct DrawSmem {
   float xp[kMaxK];
   float xq[kMaxK];
   int bad, n, kb, last;
-  DF red[kDWarps][4];
   DF wsum[kDWarps];
+  DF wsum4[kDWarps][4];
   struct {
     int jstar, mode, last_mode, pick, lastpos, token;
     unsigned long long best;
     DF tg, dc;
   } loc;
+  int pick2;   // tile-level pick
+  int lastj;
 };
 
 __device__ __forceinline__ void dflag(const DrawArgs& a, unsigned f) { atomicOr(a.err, f); }
@@ -136,8 +137,7 @@ __device__ void draw_inputs(const DrawArgs& a, int b, float T, DrawSmem& sm) {
       sm.xq[lane] = E::load_scalar(a.draft, ((long long)b * K + lane) * (long long)a.V + x);
     }
   }
-  if (!greedy)
-    for (int i = threadIdx.x; i < 256; i += kDThreads) sm.tab[i] = kExp2Table256[i];
+  for (int i = threadIdx.x; i < 256; i += kDThreads) sm.tab[i] = kExp2Table256[i];
 }
 
 // Fold the tile partials of the row's positions, one half-warp per position
@@ -228,20 +228,19 @@ __device__ void draw_scan(const DrawArgs& a, int b, float T, bool write, DrawSme
   }
 }
 
-// What weighing position n of batch row b needs.
+// What weighing position n of batch row b needs (residual: n < K_b).
 template <typename E>
-__device__ __forceinline__ SampleCtx draw_ctx(const DrawArgs& a, int b, float T, const DrawSmem& sm) {
-  const int K = a.K, n = sm.n;
-  const bool residual = n < sm.kb;
+__device__ __forceinline__ SampleCtx make_ctx(const DrawArgs& a, int b, int n, bool residual,
+                                              float MCp, float Sp32, float MCq, float Sq32, float T) {
+  const int K = a.K;
   const long long rowbytes = (long long)a.V * E::kBytes;
   SampleCtx x;
   x.rowP = (const char*)a.target + ((long long)b * (K + 1) + n) * rowbytes;
   x.rowQ = residual ? (const char*)a.draft + ((long long)b * K + n) * rowbytes : nullptr;
   x.V = a.V;
-  x.MCp = sm.rowMC[n];
-  x.MCq = residual ? sm.rowMC[K + 1 + n] : 0.f;
-  const float Sp32 = sm.rowS[n];
-  const float Sq32 = residual ? sm.rowS[K + 1 + n] : 1.f;
+  x.MCp = MCp;
+  x.MCq = residual ? MCq : 0.f;
+  if (!residual) Sq32 = 1.f;
   x.L = log2e_over(T);
   x.c_hi = x.L.hi;
   x.c_lo = x.L.lo;
@@ -254,8 +253,8 @@ __device__ __forceinline__ SampleCtx draw_ctx(const DrawArgs& a, int b, float T,
   // tested on the logit (rounded to the storage type, so that a packed
   // bf16 compare gives the same answer as a float32 one)
   const float c = log2e_over_f(T);
-  x.tp = E::round_logit(__fdiv_rn(__fadd_rn(x.MCp, __log2f(kBigProb * Sp32)), c));
-  x.tq = residual ? E::round_logit(__fdiv_rn(__fadd_rn(x.MCq, __log2f(kBigProb * Sq32)), c))
+  x.tp = E::round_logit(__fdiv_rn(__fadd_rn(MCp, __log2f(kBigProb * Sp32)), c));
+  x.tq = residual ? E::round_logit(__fdiv_rn(__fadd_rn(MCq, __log2f(kBigProb * Sq32)), c))
                   : __int_as_float(0x7f800000);
   return x;
 }
@@ -299,16 +298,14 @@ __device__ __forceinline__ uint32_t ge_bf16x2(uint32_t a, uint32_t b) {
   return m;
 }
 
-// Weigh tile `tile` of the sampled row(s) (one warp) and add its totals --
-// W (weights at cw), Q (e^q where the weight is positive), P (all e^p) --
-// to tot[0..2] as warp sums, and the lane's share of S (all e^q) to tot[3].
-// Large terms (logit at or above the row's threshold) are listed and
-// weighed in double-float, one per lane, from the tile staged in shared
+// Weigh tile `tile` of the sampled row(s) (one warp) and write its record:
+// W (weights at cw), Q (e^q where the weight is positive), P and S (all e^p
+// and e^q).  Large terms (logit at or above the row's threshold) are listed
+// and weighed in double-float, one per lane, from the tile staged in shared
 // memory; in the float32 pass their logits read as -inf, so they add +0.
-// Lane 0 writes the tile's record (W, Q, P).
 template <typename E, bool kAligned, bool kResidual>
 __device__ void weigh_tile(const DrawArgs& a, DrawSmem& sm, const SampleCtx& x, int b, int tile,
-                           int lane, int warp, int full_end, DF (&tot)[4]) {
+                           int lane, int warp, int full_end) {
   constexpr int kTileElems = kTileVecs * E::kVec;
   uint32_t wp[kTileVecsPerLane][4], wq[kTileVecsPerLane][4];
   const bool ok = in_bounds(a, tile >= 0 && tile < a.tpr);
@@ -442,18 +439,15 @@ __device__ void weigh_tile(const DrawArgs& a, DrawSmem& sm, const SampleCtx& x, 
   if (kResidual) {
     Q = warp_sum_df(Q);
     P = warp_sum_df(P);
+    S = warp_sum_df(S);
   } else {
     P = W;
   }
   if (lane == 0 && ok) {
     float4* rec = a.tile_recs + 2 * ((long long)b * a.tpr + tile);
     rec[0] = make_float4(W.hi, W.lo, Q.hi, Q.lo);
-    rec[1] = make_float4(P.hi, P.lo, 0.f, 0.f);
+    rec[1] = make_float4(P.hi, P.lo, S.hi, S.lo);
   }
-  tot[0] = df_add(tot[0], W);
-  tot[1] = df_add(tot[1], Q);
-  tot[2] = df_add(tot[2], P);
-  tot[3] = df_add(tot[3], S);   // the lane's share; summed over the warp once
 }
 
 // ---------------------------------------------------------------- step 5
@@ -517,81 +511,125 @@ __device__ __forceinline__ void vec_weights(const uint32_t (&wp)[4], const uint3
   }
 }
 
-// The CTA holding the row's last ticket, warp 0: choose the part by the
-// prefix of the part records, then the tile by the prefix of that part's
-// tile records.  Leaves in sm.loc the tile, the mass left inside it, the
-// weight mode, the correction dc, and whether rounding pushed u*W to the
-// top (then the last positive element is taken).
-__device__ void locate_tile(const DrawArgs& a, DrawSmem& sm, const SampleCtx& x, int b, float u,
-                            bool residual) {
-  const int lane = threadIdx.x & 31;
-  const int G = a.parts, tpr = a.tpr;
-  const float4* precs = a.part_recs + 2 * (long long)b * kMaxParts;
-  const float4* trecs = reinterpret_cast<const float4*>(&sm.stage[0][0][0]);   // staged by the CTA
-  // part records: the totals of e^p and e^q give the exact c = S_p / S_q
-  float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f), r1 = r0;
-  if (lane < G) {
-    r0 = __ldcg(precs + 2 * lane);
-    r1 = __ldcg(precs + 2 * lane + 1);
+// Block-wide sums of four double-floats; every thread gets the totals.
+__device__ __forceinline__ void block_sum4(DF (&v)[4], DrawSmem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = warp_sum_df(v[i]);
+  if (lane == 0)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sm.wsum4[warp][i] = v[i];
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    DF t{0.f, 0.f};
+    for (int w = 0; w < kDWarps; ++w) t = df_add(t, sm.wsum4[w][i]);
+    v[i] = t;
   }
+  __syncthreads();
+}
+
+// Block-wide inclusive prefix of one double-float per thread (exclusive in
+// exc); sm.wsum is scratch.
+__device__ __forceinline__ DF block_scan(DF own, DrawSmem& sm, DF& exc) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  DF inc = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF up = df_shfl_up(inc, o);
+    if (lane >= o) inc = df_add(inc, up);
+  }
+  if (lane == 31) sm.wsum[warp] = inc;
+  __syncthreads();
+  DF pre{0.f, 0.f};
+  for (int w = 0; w < warp; ++w) pre = df_add(pre, sm.wsum[w]);
+  exc = df_add(pre, df_sub(inc, own));
+  return df_add(pre, inc);
+}
+
+// All threads of the CTA locating row r: from the row's tile records
+// (staged in shared memory) the exact c = S_p / S_q, the corrected total,
+// u*W, and the tile holding it.  Leaves in sm.loc the tile, the mass left
+// inside it, the weight mode, the correction dc, and whether rounding
+// pushed u*W to the top (then the last positive element is taken).
+__device__ void locate_tile(const DrawArgs& a, DrawSmem& sm, const SampleCtx& x, float u,
+                            bool residual) {
+  const int tid = threadIdx.x;
+  const int tpr = a.tpr;
+  const float4* recs = reinterpret_cast<const float4*>(&sm.stage[0][0][0]);
+  const int per = (tpr + kDThreads - 1) / kDThreads;   // records per thread, contiguous
+  const int j0 = min(tpr, tid * per), j1 = min(tpr, j0 + per);
+  DF v[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+  for (int j = j0; j < j1; ++j) {
+    const float4 r0 = recs[2 * j], r1 = recs[2 * j + 1];
+    v[0] = df_add(v[0], DF{r0.x, r0.y});
+    v[1] = df_add(v[1], DF{r0.z, r0.w});
+    v[2] = df_add(v[2], DF{r1.x, r1.y});
+    v[3] = df_add(v[3], DF{r1.z, r1.w});
+  }
+  block_sum4(v, sm);   // W, Q, P, S over the row
   DF dc{0.f, 0.f};
   int mode = residual ? 0 : 1;
-  DF own{r0.x, r0.y};
+  DF tot = v[0];
   if (residual) {
-    const DF Sp = warp_sum_df(DF{r1.x, r1.y}), Sq = warp_sum_df(DF{r1.z, r1.w});
-    dc = df_sub(df_div(Sp, Sq), DF{x.cw, 0.f});
-    own = df_sub(own, df_mul(dc, DF{r0.z, r0.w}));
-  }
-  DF tot = warp_sum_df(own);
-  if (residual && !df_pos(tot)) {   // the residual is zero everywhere: draw from p_n
-    mode = 2;
-    own = DF{r1.x, r1.y};
-    tot = warp_sum_df(own);
+    dc = df_sub(df_div(v[2], v[3]), DF{x.cw, 0.f});
+    tot = df_sub(v[0], df_mul(dc, v[1]));
+    if (!df_pos(tot)) {   // the residual is zero everywhere: draw from p_n
+      mode = 2;
+      tot = v[2];
+    }
   }
   const DF tau = df_mul_f(tot, u);
-  DF tl;
-  int last;
-  const int gs = pick_lane(lane < G ? own : DF{0.f, 0.f}, tau, lane, tl, last);
-  // that part's tiles, 32 per round
-  const int t0 = gs * tpr / G, t1 = (gs + 1) * tpr / G;
-  int jstar = t0;
-  int last_mode = last;
-  DF tg = tl;
-  DF base{0.f, 0.f};
-  int lastpos = -1;
-  bool found = false;
-  for (int c0 = t0; c0 < t1 && !found; c0 += 32) {
-    const int j = c0 + lane;
-    const DF wj = j < t1 ? rec_weight(trecs, j, mode, dc) : DF{0.f, 0.f};
-    if (df_pos(wj)) lastpos = j;
-    const DF vt = warp_sum_df(wj);
-    if (!last_mode && df_lt(tg, df_add(base, vt))) {
-      DF t2;
-      int l2;
-      const int h = pick_lane(wj, df_sub(tg, base), lane, t2, l2);
-      jstar = c0 + h;
-      tg = t2;
-      last_mode = l2;
-      found = true;
+  DF own{0.f, 0.f};
+  int lastj = -1;
+  for (int j = j0; j < j1; ++j) {
+    const DF wj = rec_weight(recs, j, mode, dc);
+    if (df_pos(wj)) {
+      own = df_add(own, wj);
+      lastj = j;
     }
-    base = df_add(base, vt);
   }
-  if (!found) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, o));
-    jstar = lastpos >= 0 ? lastpos : t0;
-    last_mode = 1;
+  if (tid == 0) {
+    sm.pick2 = 0x7fffffff;
+    sm.lastj = -1;
   }
-  if (lane == 0) {
-    sm.loc.jstar = jstar;
-    sm.loc.mode = mode;
-    sm.loc.last_mode = last_mode;
+  DF exc;
+  const DF inc = block_scan(own, sm, exc);   // (its barrier orders the resets above)
+  if (df_pos(own) && df_lt(tau, inc)) atomicMin(&sm.pick2, tid);
+  if (lastj >= 0) atomicMax(&sm.lastj, lastj);
+  __syncthreads();
+  if (tid == sm.pick2) {
+    DF run = exc;
+    int js = -1, jl = -1;
+    DF tg{0.f, 0.f};
+    for (int j = j0; j < j1 && js < 0; ++j) {
+      const DF wj = rec_weight(recs, j, mode, dc);
+      if (!df_pos(wj)) continue;
+      jl = j;
+      const DF nxt = df_add(run, wj);
+      if (df_lt(tau, nxt)) {
+        js = j;
+        tg = df_sub(tau, run);
+      }
+      run = nxt;
+    }
+    sm.loc.jstar = js >= 0 ? js : jl;   // rounding inside the thread: its last positive tile
+    sm.loc.last_mode = js >= 0 ? 0 : 1;
     sm.loc.tg = tg;
+  } else if (tid == 0 && sm.pick2 == 0x7fffffff) {
+    // u*W at or past the total by rounding: the last tile with positive weight
+    sm.loc.jstar = sm.lastj >= 0 ? sm.lastj : 0;
+    sm.loc.last_mode = 1;
+    sm.loc.tg = DF{0.f, 0.f};
+  }
+  if (tid == 0) {
+    sm.loc.mode = mode;
     sm.loc.dc = dc;
     sm.loc.pick = 0x7fffffff;
     sm.loc.lastpos = -1;
     sm.loc.best = 0ull;
   }
+  __syncthreads();
 }
 
 // Order-preserving bits of a float (larger float, larger key).
@@ -705,53 +743,38 @@ __global__ void __launch_bounds__(kDThreads, 4) sv_draw_kernel(DrawArgs a) {
   if (sm.bad || greedy) return;   // the same in every part
 
   // step 4: this part's tiles of position n
-  const SampleCtx x = draw_ctx<E>(a, b, T, sm);
-  const bool residual = sm.n < sm.kb;
+  const int n = sm.n;
+  const bool residual = n < sm.kb;
+  const SampleCtx x = make_ctx<E>(a, b, n, residual, sm.rowMC[n], sm.rowS[n],
+                                  residual ? sm.rowMC[a.K + 1 + n] : 0.f,
+                                  residual ? sm.rowS[a.K + 1 + n] : 1.f, T);
   const int full_end = ((long long)a.tpr * kTileVecs * E::kVec == a.V) ? a.tpr : a.tpr - 1;
   const int t0 = g * a.tpr / G, t1 = (g + 1) * a.tpr / G;
-  DF tot[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
   for (int t = t0 + warp; t < t1; t += kDWarps) {
-    if (residual) weigh_tile<E, kAligned, true>(a, sm, x, b, t, lane, warp, full_end, tot);
-    else weigh_tile<E, kAligned, false>(a, sm, x, b, t, lane, warp, full_end, tot);
+    if (residual) weigh_tile<E, kAligned, true>(a, sm, x, b, t, lane, warp, full_end);
+    else weigh_tile<E, kAligned, false>(a, sm, x, b, t, lane, warp, full_end);
   }
-  tot[3] = warp_sum_df(tot[3]);
-  if (lane == 0)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sm.red[warp][i] = tot[i];
   __syncthreads();
-  if (warp == 0) {
-    DF v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[i] = lane < kDWarps ? sm.red[lane][i] : DF{0.f, 0.f};
-      v[i] = warp_sum_df(v[i]);
-    }
-    if (lane == 0) {
-      float4* pr = a.part_recs + 2 * ((long long)b * kMaxParts + g);
-      pr[0] = make_float4(v[0].hi, v[0].lo, v[1].hi, v[1].lo);
-      pr[1] = make_float4(v[2].hi, v[2].lo, v[3].hi, v[3].lo);
-      __threadfence();   // this part's records before its ticket
-      sm.last = atomicAdd(a.tickets + b, 1u) + 1u == (unsigned)G;
-    }
+  if (tid == 0) {
+    __threadfence();   // this part's tile records before its ticket
+    sm.last = atomicAdd(a.tickets + b, 1u) + 1u == (unsigned)G;
   }
   __syncthreads();
   if (!sm.last) return;
-  // step 5: every part's records are written; stage the row's tile records
-  // (the sweep's stage is free) so the tile choice reads shared memory
+
+  // step 5: every part's tile records are written; stage them so the tile
+  // choice reads shared memory (the sweep's stage is free)
   __threadfence();
   {
-    static_assert(sizeof(sm.stage) >= 2 * 1024 * sizeof(float4), "room for 1024 tile records");
     float4* st = reinterpret_cast<float4*>(&sm.stage[0][0][0]);
     const float4* trecs = a.tile_recs + 2 * (long long)b * a.tpr;
-    for (int i = tid; i < 2 * a.tpr; i += kDThreads)
-      st[i] = in_bounds(a, a.tpr <= 1024) ? __ldcg(trecs + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = tid; k < 2 * a.tpr; k += kDThreads)
+      st[k] = in_bounds(a, a.tpr <= 1024) ? __ldcg(trecs + k) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   __syncthreads();
-  if (warp == 0) locate_tile(a, sm, x, b, sm.r[sm.kb], residual);
-  __syncthreads();
+  locate_tile(a, sm, x, sm.r[sm.kb], residual);
   const int token = locate_element<E>(a, sm, x);
   if (warp == 0) {
-    const int n = sm.n;
     if (lane == 0) a.out_tokens[(long long)b * (a.K + 1) + n] = token;
     if (kPlug)
       plug_row(lane, n, lane < n ? sm.tok[lane] : token,

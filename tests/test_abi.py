@@ -47,13 +47,13 @@ def test_every_declared_symbol_is_exported(N):
 def _layout_bytes(B, K, V, elt):
     """The workspace layout: a 256-byte header, then 256-byte aligned
     regions -- one 8-byte partial per 2 KB tile of every target and draft
-    row, a 4-byte draw ticket per batch row, 32 part records and one record
-    per tile of the sampled row per batch row (32 bytes each)."""
+    row, a 4-byte draw ticket per batch row, and a 32-byte record per tile
+    of every batch row's sampled row."""
     al = lambda x: (x + 255) // 256 * 256
     rows = B * (2 * K + 1)
     tpr = -(-V // (2048 // elt))
     off = 256
-    for size in (rows * tpr * 8, B * 4, B * 32 * 32, B * tpr * 32):
+    for size in (rows * tpr * 8, B * 4, B * tpr * 32):
         off = al(off + size)
     return off
 
