@@ -234,6 +234,27 @@ __device__ __forceinline__ DF warp_sum_df(DF v) {
   for (int o = 16; o > 0; o >>= 1) v = df_add(v, df_shfl_xor(v, o));
   return v;
 }
+// Warp sums of four double-floats at once: after the call lanes 0-7 hold
+// the sum of v0, lanes 8-15 of v1, 16-23 of v2, 24-31 of v3.  Every lane
+// exchanges and adds only what its half (then quarter) of the warp keeps.
+__device__ __forceinline__ DF warp_sum4_df(DF v0, DF v1, DF v2, DF v3) {
+  const int lane = threadIdx.x & 31;
+  const bool hi16 = (lane & 16) != 0, hi8 = (lane & 8) != 0;
+  DF a0 = hi16 ? v2 : v0, a1 = hi16 ? v3 : v1;   // kept
+  const DF b0 = hi16 ? v0 : v2, b1 = hi16 ? v1 : v3;   // given to lane ^ 16
+  a0 = df_add(a0, df_shfl_xor(b0, 16));
+  a1 = df_add(a1, df_shfl_xor(b1, 16));
+  DF c = hi8 ? a1 : a0;
+  const DF d = hi8 ? a0 : a1;   // given to lane ^ 8
+  c = df_add(c, df_shfl_xor(d, 8));
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) c = df_add(c, df_shfl_xor(c, o));
+  return c;
+}
+// Prefetch the 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 
 // log2(e) / T as a double-float: the float32 quotient plus the correctly
 // signed remainder divided by T.

@@ -435,18 +435,15 @@ __device__ void weigh_tile(const DrawArgs& a, DrawSmem& sm, const SampleCtx& x, 
       }
     }
   }
-  W = warp_sum_df(W);
+  // the record: (W, Q), (P, S) as double-floats, one 8-byte store per total
+  float2* rec = reinterpret_cast<float2*>(a.tile_recs + 2 * ((long long)b * a.tpr + tile));
   if (kResidual) {
-    Q = warp_sum_df(Q);
-    P = warp_sum_df(P);
-    S = warp_sum_df(S);
+    const DF tot = warp_sum4_df(W, Q, P, S);   // lanes 0, 8, 16, 24 hold W, Q, P, S
+    if ((lane & 7) == 0 && ok) rec[lane >> 3] = make_float2(tot.hi, tot.lo);
   } else {
-    P = W;
-  }
-  if (lane == 0 && ok) {
-    float4* rec = a.tile_recs + 2 * ((long long)b * a.tpr + tile);
-    rec[0] = make_float4(W.hi, W.lo, Q.hi, Q.lo);
-    rec[1] = make_float4(P.hi, P.lo, S.hi, S.lo);
+    W = warp_sum_df(W);   // P = W, no Q or S
+    if (lane < 4 && ok)
+      rec[lane] = (lane & 1) ? make_float2(0.f, 0.f) : make_float2(W.hi, W.lo);
   }
 }
 
@@ -750,6 +747,17 @@ __global__ void __launch_bounds__(kDThreads, 4) sv_draw_kernel(DrawArgs a) {
                                   residual ? sm.rowS[a.K + 1 + n] : 1.f, T);
   const int full_end = ((long long)a.tpr * kTileVecs * E::kVec == a.V) ? a.tpr : a.tpr - 1;
   const int t0 = g * a.tpr / G, t1 = (g + 1) * a.tpr / G;
+  // every tile after each warp's first goes to L2 now (lanes 0-15 the target
+  // row's 16 lines of it, lanes 16-31 the draft row's), so that the part's
+  // whole re-read is in flight at once
+  {
+    const long long rowbytes = (long long)a.V * E::kBytes;
+    const char* row = lane < 16 ? x.rowP : x.rowQ;
+    for (int t = t0 + warp + kDWarps; t < t1; t += kDWarps) {
+      const long long off = (long long)t * kTileVecs * 16 + 128 * (lane & 15);
+      if (off < rowbytes && (lane < 16 || residual)) prefetch_l2(row + off);
+    }
+  }
   for (int t = t0 + warp; t < t1; t += kDWarps) {
     if (residual) weigh_tile<E, kAligned, true>(a, sm, x, b, t, lane, warp, full_end);
     else weigh_tile<E, kAligned, false>(a, sm, x, b, t, lane, warp, full_end);
