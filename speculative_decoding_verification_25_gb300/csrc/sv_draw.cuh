@@ -81,14 +81,11 @@ struct DrawSmem {
   float xq[kMaxK];
   int bad, n, kb, last;
   DF wsum[kDWarps];
-  DF wsum4[kDWarps][4];
   struct {
     int jstar, mode, last_mode, pick, lastpos, token;
     unsigned long long best;
     DF tg, dc;
   } loc;
-  int pick2;   // tile-level pick
-  int lastj;
 };
 
 __device__ __forceinline__ void dflag(const DrawArgs& a, unsigned f) { atomicOr(a.err, f); }
@@ -508,24 +505,6 @@ __device__ __forceinline__ void vec_weights(const uint32_t (&wp)[4], const uint3
   }
 }
 
-// Block-wide sums of four double-floats; every thread gets the totals.
-__device__ __forceinline__ void block_sum4(DF (&v)[4], DrawSmem& sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = warp_sum_df(v[i]);
-  if (lane == 0)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sm.wsum4[warp][i] = v[i];
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    DF t{0.f, 0.f};
-    for (int w = 0; w < kDWarps; ++w) t = df_add(t, sm.wsum4[w][i]);
-    v[i] = t;
-  }
-  __syncthreads();
-}
-
 // Block-wide inclusive prefix of one double-float per thread (exclusive in
 // exc); sm.wsum is scratch.
 __device__ __forceinline__ DF block_scan(DF own, DrawSmem& sm, DF& exc) {
@@ -544,36 +523,41 @@ __device__ __forceinline__ DF block_scan(DF own, DrawSmem& sm, DF& exc) {
   return df_add(pre, inc);
 }
 
-// All threads of the CTA locating row r: from the row's tile records
-// (staged in shared memory) the exact c = S_p / S_q, the corrected total,
-// u*W, and the tile holding it.  Leaves in sm.loc the tile, the mass left
-// inside it, the weight mode, the correction dc, and whether rounding
-// pushed u*W to the top (then the last positive element is taken).
-__device__ void locate_tile(const DrawArgs& a, DrawSmem& sm, const SampleCtx& x, float u,
+// Warp 0 of the locating CTA: from the row's tile records (staged in
+// shared memory) the exact c = S_p / S_q, the corrected total, u*W, and the
+// tile holding it; lane l takes the records [l*per, (l+1)*per).  Leaves in
+// sm.loc the tile, the mass left inside it, the weight mode, the
+// correction dc, and whether rounding pushed u*W to the top (then the last
+// positive element is taken).
+__device__ void choose_tile(const DrawArgs& a, DrawSmem& sm, const SampleCtx& x, float u,
                             bool residual) {
-  const int tid = threadIdx.x;
+  const int lane = threadIdx.x & 31;
   const int tpr = a.tpr;
   const float4* recs = reinterpret_cast<const float4*>(&sm.stage[0][0][0]);
-  const int per = (tpr + kDThreads - 1) / kDThreads;   // records per thread, contiguous
-  const int j0 = min(tpr, tid * per), j1 = min(tpr, j0 + per);
-  DF v[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+  const int per = (tpr + 31) / 32;
+  const int j0 = min(tpr, lane * per), j1 = min(tpr, j0 + per);
+  DF v0{0.f, 0.f}, v1{0.f, 0.f}, v2{0.f, 0.f}, v3{0.f, 0.f};
   for (int j = j0; j < j1; ++j) {
     const float4 r0 = recs[2 * j], r1 = recs[2 * j + 1];
-    v[0] = df_add(v[0], DF{r0.x, r0.y});
-    v[1] = df_add(v[1], DF{r0.z, r0.w});
-    v[2] = df_add(v[2], DF{r1.x, r1.y});
-    v[3] = df_add(v[3], DF{r1.z, r1.w});
+    v0 = df_add(v0, DF{r0.x, r0.y});
+    v1 = df_add(v1, DF{r0.z, r0.w});
+    v2 = df_add(v2, DF{r1.x, r1.y});
+    v3 = df_add(v3, DF{r1.z, r1.w});
   }
-  block_sum4(v, sm);   // W, Q, P, S over the row
+  const DF t4 = warp_sum4_df(v0, v1, v2, v3);   // W, Q, P, S over the row at lanes 0, 8, 16, 24
+  const DF Wt{__shfl_sync(0xffffffffu, t4.hi, 0), __shfl_sync(0xffffffffu, t4.lo, 0)};
   DF dc{0.f, 0.f};
   int mode = residual ? 0 : 1;
-  DF tot = v[0];
+  DF tot = Wt;
   if (residual) {
-    dc = df_sub(df_div(v[2], v[3]), DF{x.cw, 0.f});
-    tot = df_sub(v[0], df_mul(dc, v[1]));
+    const DF Qt{__shfl_sync(0xffffffffu, t4.hi, 8), __shfl_sync(0xffffffffu, t4.lo, 8)};
+    const DF Pt{__shfl_sync(0xffffffffu, t4.hi, 16), __shfl_sync(0xffffffffu, t4.lo, 16)};
+    const DF St{__shfl_sync(0xffffffffu, t4.hi, 24), __shfl_sync(0xffffffffu, t4.lo, 24)};
+    dc = df_sub(df_div(Pt, St), DF{x.cw, 0.f});
+    tot = df_sub(Wt, df_mul(dc, Qt));
     if (!df_pos(tot)) {   // the residual is zero everywhere: draw from p_n
       mode = 2;
-      tot = v[2];
+      tot = Pt;
     }
   }
   const DF tau = df_mul_f(tot, u);
@@ -586,17 +570,11 @@ __device__ void locate_tile(const DrawArgs& a, DrawSmem& sm, const SampleCtx& x,
       lastj = j;
     }
   }
-  if (tid == 0) {
-    sm.pick2 = 0x7fffffff;
-    sm.lastj = -1;
-  }
-  DF exc;
-  const DF inc = block_scan(own, sm, exc);   // (its barrier orders the resets above)
-  if (df_pos(own) && df_lt(tau, inc)) atomicMin(&sm.pick2, tid);
-  if (lastj >= 0) atomicMax(&sm.lastj, lastj);
-  __syncthreads();
-  if (tid == sm.pick2) {
-    DF run = exc;
+  DF tl;
+  int past;
+  const int h = pick_lane(own, tau, lane, tl, past);
+  if (!past && lane == h) {
+    DF run{0.f, 0.f};
     int js = -1, jl = -1;
     DF tg{0.f, 0.f};
     for (int j = j0; j < j1 && js < 0; ++j) {
@@ -604,29 +582,33 @@ __device__ void locate_tile(const DrawArgs& a, DrawSmem& sm, const SampleCtx& x,
       if (!df_pos(wj)) continue;
       jl = j;
       const DF nxt = df_add(run, wj);
-      if (df_lt(tau, nxt)) {
+      if (df_lt(tl, nxt)) {
         js = j;
-        tg = df_sub(tau, run);
+        tg = df_sub(tl, run);
       }
       run = nxt;
     }
-    sm.loc.jstar = js >= 0 ? js : jl;   // rounding inside the thread: its last positive tile
+    sm.loc.jstar = js >= 0 ? js : jl;   // rounding inside the lane: its last positive tile
     sm.loc.last_mode = js >= 0 ? 0 : 1;
     sm.loc.tg = tg;
-  } else if (tid == 0 && sm.pick2 == 0x7fffffff) {
-    // u*W at or past the total by rounding: the last tile with positive weight
-    sm.loc.jstar = sm.lastj >= 0 ? sm.lastj : 0;
-    sm.loc.last_mode = 1;
-    sm.loc.tg = DF{0.f, 0.f};
   }
-  if (tid == 0) {
+  if (past) {   // u*W at or past the total by rounding: the last tile with positive weight
+    int lj = lastj;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lj = max(lj, __shfl_xor_sync(0xffffffffu, lj, o));
+    if (lane == 0) {
+      sm.loc.jstar = lj >= 0 ? lj : 0;
+      sm.loc.last_mode = 1;
+      sm.loc.tg = DF{0.f, 0.f};
+    }
+  }
+  if (lane == 0) {
     sm.loc.mode = mode;
     sm.loc.dc = dc;
     sm.loc.pick = 0x7fffffff;
     sm.loc.lastpos = -1;
     sm.loc.best = 0ull;
   }
-  __syncthreads();
 }
 
 // Order-preserving bits of a float (larger float, larger key).
@@ -764,15 +746,17 @@ __global__ void __launch_bounds__(kDThreads, 4) sv_draw_kernel(DrawArgs a) {
   }
   __syncthreads();
   if (tid == 0) {
-    __threadfence();   // this part's tile records before its ticket
-    sm.last = atomicAdd(a.tickets + b, 1u) + 1u == (unsigned)G;
+    // release: this part's tile records (written before the barrier) before
+    // its ticket; acquire: the last part sees every part's records
+    unsigned prev;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(prev) : "l"(a.tickets + b) : "memory");
+    sm.last = prev + 1u == (unsigned)G;
   }
   __syncthreads();
   if (!sm.last) return;
 
   // step 5: every part's tile records are written; stage them so the tile
   // choice reads shared memory (the sweep's stage is free)
-  __threadfence();
   {
     float4* st = reinterpret_cast<float4*>(&sm.stage[0][0][0]);
     const float4* trecs = a.tile_recs + 2 * (long long)b * a.tpr;
@@ -780,7 +764,8 @@ __global__ void __launch_bounds__(kDThreads, 4) sv_draw_kernel(DrawArgs a) {
       st[k] = in_bounds(a, a.tpr <= 1024) ? __ldcg(trecs + k) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   __syncthreads();
-  locate_tile(a, sm, x, sm.r[sm.kb], residual);
+  if (warp == 0) choose_tile(a, sm, x, sm.r[sm.kb], residual);
+  __syncthreads();
   const int token = locate_element<E>(a, sm, x);
   if (warp == 0) {
     if (lane == 0) a.out_tokens[(long long)b * (a.K + 1) + n] = token;
