@@ -515,10 +515,12 @@ def bench_workload(args, name, rank, world, local):
     p1_bytes, p2_bytes = algorithmic_bytes(w, accepted)
     hbm, peak_src = peaks()
     step_gbs = (p1_bytes + p2_bytes) / (ms_per_step * 1e-3) / 1e9
-    t1, t2 = stored_traffic(name, "sv_row_stats_kernel"), stored_traffic(name, "sv_draw_kernel")
+    # the streaming kernel a ragged batch of up to 2048 rows runs is the compact one
+    k1 = "sv_row_stats_compact_kernel" if ragged and B <= 2048 else "sv_row_stats_kernel"
+    t1, t2 = stored_traffic(name, k1), stored_traffic(name, "sv_draw_kernel")
     roofline = {"bound": "hbm", "achieved": step_gbs, "peak": hbm, "unit": "GB/s",
                 "frac": step_gbs / hbm, "traffic": t1 + t2 if t1 and t2 else None,
-                "kernel": "the whole step: sv_row_stats_kernel + sv_draw_kernel, back to back",
+                "kernel": f"the whole step: {k1} + sv_draw_kernel, back to back",
                 "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_src == "measured" else "fallback",
                 "bytes_per_launch": p1_bytes + p2_bytes,

@@ -198,7 +198,7 @@ int spec_verify_device_errors(const void* workspace, void* stream, uint32_t* fla
  * (256-byte aligned) in this library.  Shapes whose
  * spec_verify_workspace_bytes(B, K, V, dtype) exceeds that size are
  * rejected with SV_ERR_TOO_LARGE before anything touches the device (at
- * V = 128256 bf16 and K = 4 that admits B up to 637).  Nothing in the
+ * V = 128256 bf16 and K = 4 that admits B up to 639).  Nothing in the
  * scratch must start at zero: the streaming launch resets its flag word and
  * tickets and writes every partial before the draw launch reads it.
  *
@@ -289,8 +289,8 @@ int spec_verify_plug(const int32_t* accepted_len, const int32_t* out_tokens, int
 
 /*
  * spec_verify (or spec_verify_ragged) with the plug step fused into its
- * launch: one call, one launch, no second launch for the plug.  The warp
- * that writes a row's last token also appends the row's emitted tokens to
+ * draw launch: one call, the same two launches as spec_verify, no third
+ * launch for the plug.  The warp that writes a row's last token also appends the row's emitted tokens to
  * `tokens` and advances `seq_len`, with exactly
  * spec_verify_plug's rule: same arguments (tokens, seq_len, max_len,
  * last_token), same results.  Its SV_DEV_PLUG_CLIPPED / SV_DEV_BAD_LENGTH

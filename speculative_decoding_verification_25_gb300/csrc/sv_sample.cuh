@@ -1,6 +1,6 @@
 // Sampling arithmetic of spec_verify: the weight of one vocabulary element
 // at the sampled position, as the tile sweep and the locate step of the
-// verify kernel (sv_fused.cuh) both compute it, and the fold of tile
+// draw kernel (sv_draw.cuh) both compute it, and the fold of tile
 // partials into a row's argmax that the tree verification uses.
 //
 // The rule is the exact rejection rule of the lesson "Decodificação
