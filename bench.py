@@ -459,6 +459,40 @@ def bench_workload(args, name, rank, world, local):
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = d2h_acc.numel() * 4 + d2h_tok.numel() * 4
 
+    # ---- the streaming launch alone (spec_verify_row_stats), back to back on
+    # the same cold inputs: the pass's own throughput, outside the step
+    n_rs = max(args.steps, 50)
+    kpr = lambda c: c["k_per_row"].data_ptr() if ragged else 0
+    r0 = torch.cuda.Event(enable_timing=True)
+    r1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    if rotate:
+        r0.record(stream)
+        for i in range(n_rs):
+            c = copies[i % len(copies)]
+            if N.spec_verify_row_stats_raw(c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
+                                           c["temperature"].data_ptr(), kpr(c), B, K, V,
+                                           ws.data_ptr(), ws_bytes, sh) != N.SV_OK:
+                raise RuntimeError("spec_verify_row_stats failed")
+        r1.record(stream)
+        barrier()
+        rs_ms = r0.elapsed_time(r1) / n_rs
+    else:
+        rs_ms = 0.0
+        for i in range(n_rs):
+            flush.fill_(i & 0xff)
+            r0.record(stream)
+            c = copies[0]
+            if N.spec_verify_row_stats_raw(c["target"].data_ptr(), c["draft"].data_ptr(), dtype_code,
+                                           c["temperature"].data_ptr(), kpr(c), B, K, V,
+                                           ws.data_ptr(), ws_bytes, sh) != N.SV_OK:
+                raise RuntimeError("spec_verify_row_stats failed")
+            r1.record(stream)
+            barrier()
+            rs_ms += r0.elapsed_time(r1)
+        rs_ms /= n_rs
+    rs_ms = max_over_ranks(rs_ms, world)
+
     # ---- the plug step: on its own, and fused into the verify launch
     max_len = 4096
     seqs = torch.zeros(B, max_len, dtype=torch.int32, device=dev)
@@ -557,6 +591,13 @@ def bench_workload(args, name, rank, world, local):
         "gpu_launches": gpu_launches,
         "clocks": clocks,
         "extra": {"rows_per_s": B * world / (ms_per_step * 1e-3),
+                  "streaming_pass_alone": {
+                      "us_per_launch": rs_ms * 1e3,
+                      "gb_per_s": p1_all / (rs_ms * 1e-3) / 1e9,
+                      "frac": p1_all / (rs_ms * 1e-3) / 1e9 / hbm,
+                      "how": ("spec_verify_row_stats launched back to back on the rotating copies, "
+                              "events around the loop" if rotate else
+                              "spec_verify_row_stats timed one launch at a time after a 2 x L2 flush")},
                   "gb_per_s": step_gbs,
                   "frac_of_nominal_8tbs": step_gbs / 8000.0,
                   "pass1_bytes": p1_bytes, "resample_bytes": p2_bytes,

@@ -171,6 +171,23 @@ int spec_verify_ragged(const void* target_logits, const void* draft_logits, int 
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The streaming launch of spec_verify alone.  Every logit row that
+ * spec_verify (k_per_row == NULL) or spec_verify_ragged (k_per_row given)
+ * reads is read once, and one partial per 2 KB tile of it is written to
+ * `workspace` (at least spec_verify_workspace_bytes(B, K, V, dtype)
+ * bytes); the flag word and the draw tickets are cleared.  The partials
+ * are the library's internal intermediate, the ones spec_verify's second
+ * launch folds: this call produces no output of the step and exists to
+ * time or profile the streaming pass on its own.  Arguments as in
+ * spec_verify_ragged; draft_tokens, uniforms and the outputs are not
+ * needed.  Returns SV_OK, SV_ERR_DTYPE, SV_ERR_SHAPE, SV_ERR_NULL,
+ * SV_ERR_ALIGN, SV_ERR_WORKSPACE or SV_ERR_CUDA.
+ */
+int spec_verify_row_stats(const void* target_logits, const void* draft_logits, int dtype,
+                          const float* temperature, const int32_t* k_per_row, int B, int K, int V,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Reads the device-side row flags (SV_DEV_*) that the last spec_verify call
  * on this workspace OR-ed in.  Enqueues a 4-byte copy on `stream` and
  * SYNCHRONISES that stream; `flags` is a HOST pointer.  Returns SV_OK,

@@ -56,6 +56,7 @@ _SIG = {
     "spec_verify_and_plug": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                                   _I, _P, _P, ctypes.c_size_t, _P]),
     "spec_verify_status_string": (ctypes.c_char_p, [_I]),
+    "spec_verify_row_stats": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _P, ctypes.c_size_t, _P]),
 }
 
 _lib = None
@@ -122,6 +123,14 @@ def spec_verify_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr, temp
                                   temperature_ptr, B, K, V, accepted_ptr, out_tokens_ptr,
                                   logp_ptr, logq_ptr, workspace_ptr, workspace_bytes,
                                   stream_handle))
+
+
+def spec_verify_row_stats_raw(target_ptr, draft_ptr, dtype, temperature_ptr, k_per_row_ptr, B, K,
+                              V, workspace_ptr, workspace_bytes, stream_handle) -> int:
+    """The streaming launch of spec_verify alone (k_per_row_ptr 0: all K)."""
+    return int(load().spec_verify_row_stats(target_ptr, draft_ptr, dtype, temperature_ptr,
+                                            k_per_row_ptr or None, B, K, V, workspace_ptr,
+                                            workspace_bytes, stream_handle))
 
 
 def spec_verify_ragged_raw(target_ptr, draft_ptr, dtype, tokens_ptr, uniforms_ptr,

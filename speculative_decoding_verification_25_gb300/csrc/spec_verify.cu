@@ -401,6 +401,26 @@ int spec_verify_and_plug(const void* target_logits, const void* draft_logits, in
                        dc, (cudaStream_t)stream, plug);
 }
 
+int spec_verify_row_stats(const void* target_logits, const void* draft_logits, int dtype,
+                          const float* temperature, const int32_t* k_per_row, int B, int K, int V,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (!shape_ok(B, K, V, dtype)) return SV_ERR_SHAPE;
+  if (B == 0) return SV_OK;
+  if (!target_logits || !draft_logits || !temperature || !workspace) return SV_ERR_NULL;
+  const size_t elt = (size_t)elt_of(dtype);
+  if (!aligned_to(target_logits, elt) || !aligned_to(draft_logits, elt) ||
+      !aligned_to(temperature, 4) || !aligned_to(workspace, 16) || !aligned_to(k_per_row, 4))
+    return SV_ERR_ALIGN;
+  if (workspace_bytes < spec_verify_workspace_bytes(B, K, V, dtype)) return SV_ERR_WORKSPACE;
+  DeviceCache* dc = current_device_cache();
+  if (!dc) return SV_ERR_CUDA;
+  const Layout L = layout(B, K, V, dtype);
+  return launch_row_stats(target_logits, draft_logits, dtype, temperature, k_per_row, B, K, V,
+                          workspace, (unsigned*)((char*)workspace + L.counters), dc,
+                          (cudaStream_t)stream);
+}
+
 int spec_verify_ragged(const void* target_logits, const void* draft_logits, int dtype,
                        const int32_t* draft_tokens, const float* uniforms, const float* temperature,
                        const int32_t* k_per_row, int B, int K, int V, int32_t* accepted_len,

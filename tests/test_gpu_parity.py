@@ -125,6 +125,51 @@ def test_shapes_change_on_one_workspace():
         _assert_parity(rep, 0)
 
 
+@pytest.mark.parametrize("name,rows", [("llama3_stochastic", range(8)), ("llama3_ragged", range(12)),
+                                       ("tiny_stochastic", None), ("greedy_batch", range(5))])
+def test_row_stats_alone_leaves_the_partials_the_step_folds(name, rows):
+    """spec_verify_row_stats writes, for every row the step reads, the same
+    tile partials (bit for bit) as the first launch of spec_verify."""
+    import torch
+    from speculative_decoding_verification_25_gb300 import _native as N
+    w = synth.make(name, seed=4, rows=rows)
+    d = device_tensors(w)
+    dt = N.SV_BF16 if w.dtype == "bf16" else N.SV_F32
+    B, K, V = w.B, w.K, w.V
+    nb = N.spec_verify_workspace_bytes(B, K, V, dt)
+    sh = torch.cuda.current_stream().cuda_stream
+    kp = d["k_per_row"].data_ptr() if "k_per_row" in d else 0
+    ws1 = torch.full((nb,), 0x5A, dtype=torch.uint8, device="cuda:0")
+    ws2 = torch.full((nb,), 0xA5, dtype=torch.uint8, device="cuda:0")
+    assert N.spec_verify_row_stats_raw(d["target"].data_ptr(), d["draft"].data_ptr(), dt,
+                                       d["temperature"].data_ptr(), kp, B, K, V, ws1.data_ptr(),
+                                       nb, sh) == N.SV_OK
+    acc = torch.empty(B, dtype=torch.int32, device="cuda:0")
+    out = torch.empty(B, K + 1, dtype=torch.int32, device="cuda:0")
+    args = (d["draft_tokens"].data_ptr(), d["uniforms"].data_ptr(), d["temperature"].data_ptr())
+    if kp:
+        st = N.spec_verify_ragged_raw(d["target"].data_ptr(), d["draft"].data_ptr(), dt, *args, kp,
+                                      B, K, V, acc.data_ptr(), out.data_ptr(), None, None,
+                                      ws2.data_ptr(), nb, sh)
+    else:
+        st = N.spec_verify_raw(d["target"].data_ptr(), d["draft"].data_ptr(), dt, *args, B, K, V,
+                               acc.data_ptr(), out.data_ptr(), None, None, ws2.data_ptr(), nb, sh)
+    assert st == N.SV_OK
+    torch.cuda.synchronize()
+    a, b = ws1.cpu().numpy(), ws2.cpu().numpy()
+    assert a[:4].view(np.uint32)[0] == 0 and b[:4].view(np.uint32)[0] == 0   # no device flags
+    tpr = -(-V // (2048 // (2 if w.dtype == "bf16" else 4)))
+    kb = w.k_per_row if getattr(w, "k_per_row", None) is not None else np.full(B, K)
+    read = []
+    for r in range(B):
+        read += [r * (K + 1) + t for t in range(kb[r] + 1)]
+        if w.temperature[r] > 0:
+            read += [B * (K + 1) + r * K + t for t in range(kb[r])]
+    for row in read:
+        o = 256 + row * tpr * 8
+        np.testing.assert_array_equal(a[o:o + tpr * 8], b[o:o + tpr * 8], err_msg=f"row {row}")
+
+
 # ---------------------------------------------------------------- small shapes and edges
 
 def _random_workload(rng, B, K, V, dtype, temps, neg_inf=False, ties=False):
