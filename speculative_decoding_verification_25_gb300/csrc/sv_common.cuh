@@ -251,10 +251,6 @@ __device__ __forceinline__ DF warp_sum4_df(DF v0, DF v1, DF v2, DF v3) {
   for (int o = 4; o > 0; o >>= 1) c = df_add(c, df_shfl_xor(c, o));
   return c;
 }
-// Prefetch the 128-byte line holding p into L2.
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
 
 // log2(e) / T as a double-float: the float32 quotient plus the correctly
 // signed remainder divided by T.

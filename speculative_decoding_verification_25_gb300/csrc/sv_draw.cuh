@@ -732,14 +732,7 @@ __global__ void __launch_bounds__(kDThreads, 4) sv_draw_kernel(DrawArgs a) {
   // every tile after each warp's first goes to L2 now (lanes 0-15 the target
   // row's 16 lines of it, lanes 16-31 the draft row's), so that the part's
   // whole re-read is in flight at once
-  {
-    const long long rowbytes = (long long)a.V * E::kBytes;
-    const char* row = lane < 16 ? x.rowP : x.rowQ;
-    for (int t = t0 + warp + kDWarps; t < t1; t += kDWarps) {
-      const long long off = (long long)t * kTileVecs * 16 + 128 * (lane & 15);
-      if (off < rowbytes && (lane < 16 || residual)) prefetch_l2(row + off);
-    }
-  }
+
   for (int t = t0 + warp; t < t1; t += kDWarps) {
     if (residual) weigh_tile<E, kAligned, true>(a, sm, x, b, t, lane, warp, full_end);
     else weigh_tile<E, kAligned, false>(a, sm, x, b, t, lane, warp, full_end);
