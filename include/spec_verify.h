@@ -229,14 +229,24 @@ int spec_verify_device_errors(const void* workspace, void* stream, uint32_t* fla
  * (different streams without an ordering between them, or several host
  * threads) race on it and may return wrong tokens.  Order all calls on a
  * device, e.g. on one stream.  The device row flags of these calls are
- * kept in that scratch and are not readable through this interface; error
- * rows still show as accepted_len = -1.
+ * kept in that scratch (error rows still show as accepted_len = -1); read
+ * them with spec_verify_static_device_errors.
  */
 int spec_verify_static(const void* target_logits, const void* draft_logits, int dtype,
                        const int32_t* draft_tokens, const float* uniforms,
                        const float* temperature, int B, int K, int V,
                        int32_t* accepted_len, int32_t* out_tokens,
                        float* logp_out, float* logq_out, void* stream);
+
+/*
+ * The SV_DEV_* flags of the last spec_verify_static call on the current
+ * device: the 4-byte flag word of the static scratch, copied to the host
+ * pointer `flags` on `stream` (which is then synchronised).  Call it on the
+ * stream (or after the stream order) of the spec_verify_static call whose
+ * flags are wanted; a later static call overwrites them.  Returns SV_OK,
+ * SV_ERR_NULL (flags == NULL) or SV_ERR_CUDA.
+ */
+int spec_verify_static_device_errors(void* stream, uint32_t* flags);
 
 /*
  * Greedy verification of a draft tree per row.  The lesson's section

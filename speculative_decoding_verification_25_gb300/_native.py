@@ -57,6 +57,7 @@ _SIG = {
                                   _I, _P, _P, ctypes.c_size_t, _P]),
     "spec_verify_status_string": (ctypes.c_char_p, [_I]),
     "spec_verify_row_stats": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _P, ctypes.c_size_t, _P]),
+    "spec_verify_static_device_errors": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
 }
 
 _lib = None

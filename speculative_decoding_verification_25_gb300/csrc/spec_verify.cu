@@ -461,6 +461,15 @@ int spec_verify_static(const void* target_logits, const void* draft_logits, int 
                        (cudaStream_t)stream);
 }
 
+int spec_verify_static_device_errors(void* stream, uint32_t* flags) {
+  if (!flags) return SV_ERR_NULL;
+  DeviceCache* dc = current_device_cache();
+  if (!dc) return SV_ERR_CUDA;
+  void* scratch = static_scratch(dc);
+  if (!scratch) return SV_ERR_CUDA;
+  return spec_verify_device_errors(scratch, stream, flags);
+}
+
 size_t spec_verify_tree_workspace_bytes(int B, int N, int V, int dtype) {
   if (dtype != SV_F32 && dtype != SV_BF16) return 0;
   if (B < 0 || N < 1 || N > SV_MAX_TREE_NODES || V < 1 || V > spec_verify_max_vocab(dtype)) return 0;

@@ -90,3 +90,39 @@ def test_static_scratch_rejects_a_shape_beyond_its_size():
     st = N.spec_verify_static_raw(0x10000, 0x10000, N.SV_BF16, 0x10000, 0x10000, 0x10000, B, 4,
                                   128256, 0x10000, 0x10000, None, None, None)
     assert st == N.SV_ERR_TOO_LARGE
+
+
+def test_static_device_flags_are_readable():
+    """spec_verify_static_device_errors returns the flags of the last static
+    call: a bad temperature and a bad token raise theirs, a clean call
+    clears them."""
+    import ctypes
+    import torch
+    from speculative_decoding_verification_25_gb300 import _native as N
+    lib = N.load()
+    w = synth.make("llama3_stochastic", seed=6, rows=range(6))
+    stream = torch.cuda.current_stream().cuda_stream
+    B, K, V = w.B, w.K, w.V
+
+    def run(temps, tokens):
+        d = device_tensors(w)
+        d["temperature"].copy_(torch.tensor(temps, dtype=torch.float32))
+        d["draft_tokens"].copy_(torch.from_numpy(tokens))
+        outs = _outputs(B, K, "cuda:0")
+        st = N.spec_verify_static_raw(d["target"].data_ptr(), d["draft"].data_ptr(), N.SV_BF16,
+                                      d["draft_tokens"].data_ptr(), d["uniforms"].data_ptr(),
+                                      d["temperature"].data_ptr(), B, K, V,
+                                      *[t.data_ptr() for t in outs], stream)
+        assert st == N.SV_OK, N.status_string(st)
+        flags = ctypes.c_uint32(0xFFFFFFFF)
+        assert lib.spec_verify_static_device_errors(stream, ctypes.byref(flags)) == N.SV_OK
+        return int(flags.value), outs[0].cpu().numpy()
+
+    bad_tokens = w.draft_tokens.copy()
+    bad_tokens[3, 1] = V
+    flags, acc = run([1.0, -1.0, 1.0, 1.0, 0.0, 1.0], bad_tokens)
+    assert flags == N.SV_DEV_BAD_TEMPERATURE | N.SV_DEV_BAD_TOKEN
+    assert acc[1] == -1 and acc[3] == -1 and (np.delete(acc, [1, 3]) >= 0).all()
+    flags, acc = run(list(w.temperature), w.draft_tokens)
+    assert flags == 0 and (acc >= 0).all()
+    assert lib.spec_verify_static_device_errors(stream, None) == N.SV_ERR_NULL
