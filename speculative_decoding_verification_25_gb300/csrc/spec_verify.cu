@@ -10,8 +10,9 @@
 //      the rows read;
 //   2. sv_draw_kernel (sv_draw.cuh), G CTAs per batch row: statistics fold,
 //      acceptance scan, and the draw over the sampled position's tiles.
-// spec_verify_tree runs the first kernel over the target slots and then
-// sv_tree_kernel; spec_verify_plug is one small launch of its own.
+// spec_verify_row_stats is the first launch alone.  spec_verify_tree runs
+// the first kernel over the target slots and then sv_tree_kernel;
+// spec_verify_plug is one small launch of its own.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>

@@ -20,8 +20,9 @@
 //      one record per tile (totals of w, of the e^q under positive w, of
 //      e^p and of e^q, as double-floats);
 //   5. takes a ticket on the row; the CTA holding the last one locates the
-//      token: the tile by a block-wide scan of the row's tile records, the
-//      element by a block-wide scan of that tile, re-read.
+//      token: the tile by a warp scan over the row's tile records (staged
+//      in shared memory), the element by a block-wide scan of that tile,
+//      re-read.
 // Greedy rows (T = 0) and error rows are finished by part 0 in step 3.
 // No CTA waits on another: the ticket is one atomic per CTA.
 //
@@ -483,44 +484,6 @@ __device__ __forceinline__ int pick_lane(DF w, DF tau, int lane, DF& tl, int& la
   const DF t = df_sub(tau, exc);
   tl = DF{__shfl_sync(0xffffffffu, t.hi, h), __shfl_sync(0xffffffffu, t.lo, h)};
   return h;
-}
-
-// Element weights of one 16-byte vector of the chosen tile, as the tiles
-// were weighed (mode as in rec_weight).
-template <typename E>
-__device__ __forceinline__ void vec_weights(const uint32_t (&wp)[4], const uint32_t (&wq)[4],
-                                            long long e0, int V, const SampleCtx& x,
-                                            const float2* tab, int mode, DF dc, DF (&w)[E::kVec]) {
-#pragma unroll
-  for (int k = 0; k < E::kVec; ++k) {
-    DF q{0.f, 0.f};
-    if (e0 + k >= V) {
-      w[k] = DF{0.f, 0.f};
-    } else if (mode == 0) {
-      eval_pair<true>(E::elem(wp, k), E::elem(wq, k), x, tab, w[k], q);
-      w[k] = df_sub(w[k], df_mul(dc, q));
-    } else {
-      eval_pair<false>(E::elem(wp, k), 0.f, x, tab, w[k], q);
-    }
-  }
-}
-
-// Block-wide inclusive prefix of one double-float per thread (exclusive in
-// exc); sm.wsum is scratch.
-__device__ __forceinline__ DF block_scan(DF own, DrawSmem& sm, DF& exc) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  DF inc = own;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const DF up = df_shfl_up(inc, o);
-    if (lane >= o) inc = df_add(inc, up);
-  }
-  if (lane == 31) sm.wsum[warp] = inc;
-  __syncthreads();
-  DF pre{0.f, 0.f};
-  for (int w = 0; w < warp; ++w) pre = df_add(pre, sm.wsum[w]);
-  exc = df_add(pre, df_sub(inc, own));
-  return df_add(pre, inc);
 }
 
 // Warp 0 of the locating CTA: from the row's tile records (staged in

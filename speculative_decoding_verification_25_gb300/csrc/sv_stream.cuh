@@ -22,7 +22,10 @@
 //   all tiles and skips the rows it need not read.
 //
 //   Both kernels may be launched before the preceding kernel on the stream
-//   has finished; they wait for it before their first memory access.
+//   has finished; they wait for it before their first memory access.  Right
+//   after that wait every CTA lets the next grid on the stream (the draw
+//   launch of the same call) be scheduled, and block 0 clears the flag word
+//   and the draw tickets.
 //
 // The softmax normalisers are those of the rule's p_t = softmax(target / T)
 // and q_t = softmax(draft / T) in the lesson "Decodificação Especulativa e
