@@ -780,6 +780,9 @@ def run_tree(args):
     bytes_step = B * (Nn + 1) * V * w.elt       # every slot read once, nothing re-read
     hbm, peak_src = peaks()
     gbs = bytes_step / (ms_per_step * 1e-3) / 1e9
+    t1 = stored_traffic(args.workload, "sv_row_stats_kernel")
+    t2 = stored_traffic(args.workload, "sv_tree_kernel")
+    tree_traffic = t1 + t2 if t1 and t2 else None
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline_tree(w)
@@ -795,7 +798,7 @@ def run_tree(args):
                    "l2": f"{len(copies)} rotating input copies of {w.target.nbytes / 1e6:.2f} MB",
                    "parallelism": f"{world} independent replicas, own batch per GPU"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": gbs / hbm, "traffic": None,
+                     "frac": gbs / hbm, "traffic": tree_traffic,
                      "kernel": "sv_row_stats_kernel + sv_tree_kernel (one step)",
                      "peak_source": peak_src, "bytes_per_launch": bytes_step,
                      "ms_per_launch": ms_per_step},
