@@ -692,10 +692,6 @@ __global__ void __launch_bounds__(kDThreads, 4) sv_draw_kernel(DrawArgs a) {
                                   residual ? sm.rowS[a.K + 1 + n] : 1.f, T);
   const int full_end = ((long long)a.tpr * kTileVecs * E::kVec == a.V) ? a.tpr : a.tpr - 1;
   const int t0 = g * a.tpr / G, t1 = (g + 1) * a.tpr / G;
-  // every tile after each warp's first goes to L2 now (lanes 0-15 the target
-  // row's 16 lines of it, lanes 16-31 the draft row's), so that the part's
-  // whole re-read is in flight at once
-
   for (int t = t0 + warp; t < t1; t += kDWarps) {
     if (residual) weigh_tile<E, kAligned, true>(a, sm, x, b, t, lane, warp, full_end);
     else weigh_tile<E, kAligned, false>(a, sm, x, b, t, lane, warp, full_end);
