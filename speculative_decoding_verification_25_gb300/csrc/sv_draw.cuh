@@ -41,7 +41,7 @@ namespace sv {
 
 constexpr int kDThreads = 256;
 constexpr int kDWarps = kDThreads / 32;
-constexpr int kMaxParts = 32;
+constexpr int kMaxParts = 64;
 constexpr int kDBigCap = 64;   // large terms listed per warp per tile (more: evaluated by their own lane)
 
 struct DrawArgs {
