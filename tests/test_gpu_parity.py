@@ -217,6 +217,8 @@ CASES = [
     (1, 4, 32000, "bf16", 0), (16, 2, 32000, "bf16", 0), (3, 4, 9000, "f32", 5),
     # exactly one chunk per row, and one tile more
     (5, 3, 4096, "bf16", 0), (5, 3, 4097, "bf16", 0), (5, 3, 2048, "f32", 0),
+    # the largest vocabularies accepted (1024 tiles per row) and the largest K
+    (2, 2, 1 << 20, "bf16", 0), (2, 2, 1 << 19, "f32", 0), (2, 16, 128256, "bf16", 0),
 ]
 
 
